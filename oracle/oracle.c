@@ -1,0 +1,320 @@
+/*
+ * CPU ORACLE -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, obviously correct all-pairs / single-source shortest paths on
+ * a dense distance matrix.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this; the library never does.  It shares no code,
+ * header or constant generator with the CUDA path.
+ *
+ * Problem (blocked Floyd-Warshall thesis page, 1library.co excerpt,
+ * section 4.6; Johnson/Dijkstra page, CEUR Vol-1631 pp.105-112, the
+ * notation paragraph): a weighted directed graph given as an n x n matrix,
+ * W[i][j] the weight of arc i->j, "no arc" encoded as INF, 0 on the diagonal,
+ * weights >= 0.  Output D[i][j] = minimum over all directed paths i ~> j of
+ * the sum of arc weights, INF if there is none.
+ *
+ * int32 encoding: INF = 0x3FFFFFFF.  Entries >= INF are read as INF.  All
+ * sums are formed in int64 and a sum is only kept when it is below the value
+ * it replaces, so a path whose length reaches INF is reported as INF (the
+ * encoding cannot hold it).  Floating point: computed in double, +inf for
+ * "no arc".
+ *
+ * Functions:
+ *   oracle_fw_i32 / oracle_fw_f64  -- the Floyd-Warshall recurrence as the
+ *       thesis page restates it (section 4.6, phase descriptions): for each
+ *       intermediate vertex k in order, D[i][j] = min(D[i][j], D[i][k]+D[k][j]).
+ *       No tiling.  With threads > 1 the i-loop of one k runs in parallel; that
+ *       is exact because row k and column k do not change during step k
+ *       (D[k][k] = 0).
+ *   oracle_dijkstra_* -- Dijkstra from given sources with a binary heap
+ *       (Johnson/Dijkstra page, the sequential Dijkstra operators init,
+ *       ExtractMin and RelaxEdge).  reverse != 0 runs it on the reversed graph,
+ *       which gives columns D[:, s] instead of rows.
+ *   oracle_bfs_hops -- breadth-first hop counts (reachability).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define O_INF 0x3FFFFFFFLL
+
+int oracle_has_openmp(void) {
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+/* ---------------- Floyd-Warshall ---------------- */
+
+int oracle_fw_i32(int32_t* d, int64_t n, int64_t ld, int threads) {
+    if (n < 0 || ld < n || (n > 0 && !d)) return -1;
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            if (d[i * ld + j] > O_INF) d[i * ld + j] = (int32_t)O_INF;
+    (void)threads;
+    for (int64_t k = 0; k < n; ++k) {
+        const int32_t* rowk = d + k * ld;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1) if (threads > 1)
+        for (int64_t i = 0; i < n; ++i) {
+            int32_t* rowi = d + i * ld;
+            int64_t dik = rowi[k];
+            if (dik >= O_INF) continue; /* no path i ~> k yet */
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t dkj = rowk[j];
+                if (dkj >= O_INF) continue; /* no path k ~> j yet */
+                int64_t s = dik + dkj;
+                if (s < (int64_t)rowi[j]) rowi[j] = (int32_t)s;
+            }
+        }
+    }
+    return 0;
+}
+
+/* Steps k in [k_begin, k_end) only (used to time a bounded sample). */
+int oracle_fw_i32_steps(int32_t* d, int64_t n, int64_t ld, int64_t k_begin, int64_t k_end, int threads) {
+    if (n < 0 || ld < n || k_begin < 0 || k_end > n || (n > 0 && !d)) return -1;
+    (void)threads;
+    for (int64_t k = k_begin; k < k_end; ++k) {
+        const int32_t* rowk = d + k * ld;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1) if (threads > 1)
+        for (int64_t i = 0; i < n; ++i) {
+            int32_t* rowi = d + i * ld;
+            int64_t dik = rowi[k];
+            if (dik >= O_INF) continue;
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t dkj = rowk[j];
+                if (dkj >= O_INF) continue;
+                int64_t s = dik + dkj;
+                if (s < (int64_t)rowi[j]) rowi[j] = (int32_t)s;
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_fw_f64(double* d, int64_t n, int64_t ld, int threads) {
+    if (n < 0 || ld < n || (n > 0 && !d)) return -1;
+    (void)threads;
+    for (int64_t k = 0; k < n; ++k) {
+        const double* rowk = d + k * ld;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1) if (threads > 1)
+        for (int64_t i = 0; i < n; ++i) {
+            double* rowi = d + i * ld;
+            double dik = rowi[k];
+            if (isinf(dik)) continue;
+            for (int64_t j = 0; j < n; ++j) {
+                double s = dik + rowk[j];
+                if (s < rowi[j]) rowi[j] = s;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------- graph in adjacency form ---------------- */
+
+typedef struct {
+    int64_t n;
+    int64_t* off;  /* n + 1 */
+    int32_t* dst;  /* arcs */
+    double* wf;    /* weights as double */
+    int64_t* wi;   /* weights as int64 */
+} o_graph;
+
+static void o_graph_free(o_graph* g) {
+    free(g->off); free(g->dst); free(g->wf); free(g->wi);
+    memset(g, 0, sizeof(*g));
+}
+
+/* kind: 0 = int32 matrix, 1 = float32 matrix.  reverse: arcs j->i for W[i][j]. */
+static int o_graph_build(o_graph* g, const void* w, int kind, int64_t n, int64_t ld, int reverse) {
+    memset(g, 0, sizeof(*g));
+    g->n = n;
+    g->off = (int64_t*)calloc((size_t)n + 1, sizeof(int64_t));
+    if (!g->off) return -1;
+    const int32_t* wi32 = (const int32_t*)w;
+    const float* wf32 = (const float*)w;
+#define O_HAS_ARC(i, j) ((i) != (j) && (kind == 0 ? (int64_t)wi32[(i) * ld + (j)] < O_INF \
+                                                  : !isinf(wf32[(i) * ld + (j)])))
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            if (O_HAS_ARC(i, j)) g->off[(reverse ? j : i) + 1]++;
+    for (int64_t v = 0; v < n; ++v) g->off[v + 1] += g->off[v];
+    int64_t m = g->off[n];
+    g->dst = (int32_t*)malloc(sizeof(int32_t) * (size_t)(m ? m : 1));
+    g->wf = (double*)malloc(sizeof(double) * (size_t)(m ? m : 1));
+    g->wi = (int64_t*)malloc(sizeof(int64_t) * (size_t)(m ? m : 1));
+    int64_t* fill = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n ? n : 1));
+    if (!g->dst || !g->wf || !g->wi || !fill) { free(fill); o_graph_free(g); return -1; }
+    memcpy(fill, g->off, sizeof(int64_t) * (size_t)n);
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            if (O_HAS_ARC(i, j)) {
+                int64_t from = reverse ? j : i, to = reverse ? i : j;
+                int64_t e = fill[from]++;
+                g->dst[e] = (int32_t)to;
+                if (kind == 0) { g->wi[e] = wi32[i * ld + j]; g->wf[e] = (double)wi32[i * ld + j]; }
+                else { g->wf[e] = (double)wf32[i * ld + j]; g->wi[e] = 0; }
+            }
+#undef O_HAS_ARC
+    free(fill);
+    return 0;
+}
+
+/* ---------------- binary heap of (key, vertex) ---------------- */
+
+typedef struct { double key; int64_t ikey; int32_t v; } o_item;
+typedef struct { o_item* a; int64_t size, cap; int integer; } o_heap;
+
+static int o_less(const o_heap* h, const o_item* x, const o_item* y) {
+    return h->integer ? (x->ikey < y->ikey) : (x->key < y->key);
+}
+
+static int o_push(o_heap* h, o_item it) {
+    if (h->size == h->cap) {
+        int64_t nc = h->cap ? 2 * h->cap : 1024;
+        o_item* na = (o_item*)realloc(h->a, sizeof(o_item) * (size_t)nc);
+        if (!na) return -1;
+        h->a = na; h->cap = nc;
+    }
+    int64_t c = h->size++;
+    h->a[c] = it;
+    while (c > 0) {                      /* sift up */
+        int64_t p = (c - 1) / 2;
+        if (!o_less(h, &h->a[c], &h->a[p])) break;
+        o_item t = h->a[c]; h->a[c] = h->a[p]; h->a[p] = t;
+        c = p;
+    }
+    return 0;
+}
+
+static o_item o_pop(o_heap* h) {
+    o_item top = h->a[0];
+    h->a[0] = h->a[--h->size];
+    int64_t c = 0;
+    for (;;) {                           /* sift down */
+        int64_t l = 2 * c + 1, r = l + 1, m = c;
+        if (l < h->size && o_less(h, &h->a[l], &h->a[m])) m = l;
+        if (r < h->size && o_less(h, &h->a[r], &h->a[m])) m = r;
+        if (m == c) break;
+        o_item t = h->a[c]; h->a[c] = h->a[m]; h->a[m] = t;
+        c = m;
+    }
+    return top;
+}
+
+/* One Dijkstra run: init (all INF, source 0), then repeatedly take the
+ * unsettled vertex of least tentative distance (ExtractMin) and relax its
+ * out-arcs (RelaxEdge).  Stale heap entries are skipped. */
+static int o_dijkstra_one(const o_graph* g, int64_t src, int integer, int64_t* di, double* df,
+                          unsigned char* settled) {
+    int64_t n = g->n;
+    o_heap h = {0, 0, 0, integer};
+    for (int64_t v = 0; v < n; ++v) { di[v] = INT64_MAX; df[v] = INFINITY; settled[v] = 0; }
+    di[src] = 0; df[src] = 0.0;
+    o_item s0 = {0.0, 0, (int32_t)src};
+    if (o_push(&h, s0)) return -1;
+    while (h.size > 0) {
+        o_item it = o_pop(&h);
+        int64_t u = it.v;
+        if (settled[u]) continue;
+        settled[u] = 1;
+        for (int64_t e = g->off[u]; e < g->off[u + 1]; ++e) {
+            int64_t v = g->dst[e];
+            if (integer) {
+                int64_t nd = di[u] + g->wi[e];
+                if (nd < di[v]) {
+                    di[v] = nd;
+                    o_item x = {0.0, nd, (int32_t)v};
+                    if (o_push(&h, x)) { free(h.a); return -1; }
+                }
+            } else {
+                double nd = df[u] + g->wf[e];
+                if (nd < df[v]) {
+                    df[v] = nd;
+                    o_item x = {nd, 0, (int32_t)v};
+                    if (o_push(&h, x)) { free(h.a); return -1; }
+                }
+            }
+        }
+    }
+    free(h.a);
+    return 0;
+}
+
+static int o_dijkstra_rows(const void* w, int kind, int64_t n, int64_t ld, const int32_t* sources,
+                           int64_t ns, int reverse, int32_t* out_i, double* out_f, int threads) {
+    if (n < 0 || ld < n || ns < 0 || (n > 0 && !w)) return -1;
+    for (int64_t s = 0; s < ns; ++s)
+        if (sources[s] < 0 || sources[s] >= n) return -1;
+    o_graph g;
+    if (o_graph_build(&g, w, kind, n, ld, reverse)) return -2;
+    int err = 0;
+    (void)threads;
+#pragma omp parallel num_threads(threads > 0 ? threads : 1) if (threads > 1)
+    {
+        int64_t* di = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n ? n : 1));
+        double* df = (double*)malloc(sizeof(double) * (size_t)(n ? n : 1));
+        unsigned char* st = (unsigned char*)malloc((size_t)(n ? n : 1));
+        if (!di || !df || !st) {
+#pragma omp atomic write
+            err = -2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t s = 0; s < ns; ++s) {
+                if (o_dijkstra_one(&g, sources[s], kind == 0, di, df, st)) {
+#pragma omp atomic write
+                    err = -2;
+                    continue;
+                }
+                for (int64_t v = 0; v < n; ++v) {
+                    if (kind == 0) out_i[s * n + v] = (int32_t)(di[v] < O_INF ? di[v] : O_INF);
+                    else out_f[s * n + v] = df[v];
+                }
+            }
+        }
+        free(di); free(df); free(st);
+    }
+    o_graph_free(&g);
+    return err;
+}
+
+/* Rows (or, with reverse, columns) of D for an int32 matrix; out is ns x n,
+ * INF for unreachable (and for path lengths that reach INF). */
+int oracle_dijkstra_i32(const int32_t* w, int64_t n, int64_t ld, const int32_t* sources, int64_t ns,
+                        int reverse, int32_t* out, int threads) {
+    return o_dijkstra_rows(w, 0, n, ld, sources, ns, reverse, out, NULL, threads);
+}
+
+/* Same for an fp32 matrix, accumulated in double; +inf for unreachable. */
+int oracle_dijkstra_f32(const float* w, int64_t n, int64_t ld, const int32_t* sources, int64_t ns,
+                        int reverse, double* out, int threads) {
+    return o_dijkstra_rows(w, 1, n, ld, sources, ns, reverse, NULL, out, threads);
+}
+
+/* Breadth-first hop counts from src over arcs W[i][j] < INF (int32 matrix);
+ * -1 where unreachable. */
+int oracle_bfs_hops_i32(const int32_t* w, int64_t n, int64_t ld, int64_t src, int32_t* hops) {
+    if (n <= 0 || ld < n || src < 0 || src >= n || !w || !hops) return -1;
+    int32_t* q = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+    if (!q) return -2;
+    for (int64_t v = 0; v < n; ++v) hops[v] = -1;
+    int64_t qh = 0, qt = 0;
+    hops[src] = 0; q[qt++] = (int32_t)src;
+    while (qh < qt) {
+        int64_t u = q[qh++];
+        for (int64_t v = 0; v < n; ++v)
+            if (v != u && (int64_t)w[u * ld + v] < O_INF && hops[v] < 0) {
+                hops[v] = hops[u] + 1;
+                q[qt++] = (int32_t)v;
+            }
+    }
+    free(q);
+    return 0;
+}

@@ -1,0 +1,156 @@
+"""Pins for the CPU oracle (no GPU needed).
+
+The oracle is trusted only because these pass: hand-worked graphs, brute
+force over simple paths, closed forms, breadth-first search, shortest-path
+invariants, and agreement of two independent algorithms.  The last test
+plants typical mistakes in copies of the oracle's C source and checks that
+each one makes at least one pin fail.
+"""
+
+import numpy as np
+import pytest
+
+import graphgen
+import oracle
+import pins
+
+
+def _fail_msg(bad):
+    return "\n".join(bad[:20])
+
+
+def test_golden_fixtures():
+    assert len(pins.golden_files()) >= 9
+    bad = pins.check_golden(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_brute_force_small_graphs():
+    bad = pins.check_brute_force(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_closed_forms():
+    bad = pins.check_closed_forms(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_invariants():
+    bad = pins.check_invariants(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_fw_agrees_with_dijkstra():
+    bad = pins.check_fw_vs_dijkstra(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_parallel_fw_identical_to_serial():
+    w = graphgen.er_i32(333, 0.02, 1, 1000, 5)
+    orc = oracle.default()
+    assert np.array_equal(orc.fw_i32(w, threads=1), orc.fw_i32(w, threads=4))
+    wf = graphgen.er_f32(333, 0.02, 6)
+    assert np.array_equal(orc.fw_f64(wf, threads=1), orc.fw_f64(wf, threads=4))
+
+
+def test_fw_steps_compose():
+    """Running steps [0,a) then [a,n) equals the full run."""
+    w = graphgen.er_i32(200, 0.03, 1, 100, 8)
+    orc = oracle.default()
+    d = np.minimum(w, oracle.INF_I32).astype(np.int32)
+    orc.fw_i32_steps(d, 0, 77)
+    orc.fw_i32_steps(d, 77, 200, threads=2)
+    assert np.array_equal(d, orc.fw_i32(w))
+
+
+def test_networkx_third_opinion():
+    nx = pytest.importorskip("networkx")
+    for seed, n, p in ((1, 60, 0.05), (2, 90, 0.1)):
+        w = graphgen.er_i32(n, p, 1, 50, seed)
+        g = nx.DiGraph()
+        g.add_nodes_from(range(n))
+        for i, j in zip(*np.nonzero((w < oracle.INF_I32) & ~np.eye(n, dtype=bool))):
+            g.add_edge(int(i), int(j), weight=int(w[i, j]))
+        ref = nx.floyd_warshall_numpy(g, nodelist=range(n), weight="weight")
+        ref = np.where(np.isinf(ref), oracle.INF_I32, ref).astype(np.int64)
+        assert np.array_equal(oracle.fw_i32(w).astype(np.int64), ref)
+
+
+def test_generator_splitmix64_known_value():
+    # First output of SplitMix64 seeded with 0 (published reference value).
+    assert graphgen.splitmix64_at(0, 1) == 0xE220A8397B1DCDAF
+
+
+def test_generator_shapes():
+    w = graphgen.make("er256")
+    assert w.shape == (256, 256) and np.all(np.diag(w) == 0)
+    off = w[~np.eye(256, dtype=bool)]
+    frac = np.mean(off < oracle.INF_I32)
+    assert 0.08 < frac < 0.12
+    assert off[off < oracle.INF_I32].min() >= 1 and off[off < oracle.INF_I32].max() <= 100
+    b = graphgen.ba_i32(2000, 8, 1, 1000, 4)
+    arcs = np.count_nonzero(b < oracle.INF_I32) - 2000
+    assert arcs == 2 * 8 * (2000 - 8)
+    assert np.array_equal(b < oracle.INF_I32, (b < oracle.INF_I32).T)  # two arcs per edge
+    f = graphgen.er_f32(500, 0.01, 5)
+    fo = f[~np.eye(500, dtype=bool)]
+    fin = fo[np.isfinite(fo)]
+    assert fin.min() > 0 and fin.max() <= 1.0
+    # ld > n leaves the pad columns alone
+    pad = np.full((10, 13), -7, dtype=np.int32)
+    graphgen.er_i32(10, 0.5, 1, 9, 3, ld=13, out=pad)
+    assert np.all(pad[:, 10:] == -7)
+    assert np.array_equal(pad[:, :10], graphgen.er_i32(10, 0.5, 1, 9, 3))
+
+
+# Planted mistakes: (description, original text, replacement).  Each must be
+# caught by at least one pin.  Only in-bounds mistakes are planted, so a broken
+# build cannot corrupt the test process.
+MUTANTS = [
+    ("fw: operand D[k][i] instead of D[i][k]",
+     "int64_t dik = rowi[k];", "int64_t dik = rowk[i];"),
+    ("fw: last intermediate vertex dropped",
+     "for (int64_t k = 0; k < n; ++k) {\n        const int32_t* rowk",
+     "for (int64_t k = 0; k < n - 1; ++k) {\n        const int32_t* rowk"),
+    ("fw: inputs above INF not read as INF",
+     "if (d[i * ld + j] > O_INF) d[i * ld + j] = (int32_t)O_INF;", ""),
+    ("fw: k innermost (one pass of min-plus squaring)",
+     "    for (int64_t k = 0; k < n; ++k) {\n        const int32_t* rowk = d + k * ld;\n"
+     "#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1) if (threads > 1)\n"
+     "        for (int64_t i = 0; i < n; ++i) {\n            int32_t* rowi = d + i * ld;\n"
+     "            int64_t dik = rowi[k];\n            if (dik >= O_INF) continue; /* no path i ~> k yet */\n"
+     "            for (int64_t j = 0; j < n; ++j) {\n",
+     "    for (int64_t i = 0; i < n; ++i) {\n        int32_t* rowi = d + i * ld;\n"
+     "        for (int64_t j = 0; j < n; ++j) {\n            for (int64_t k = 0; k < n; ++k) {\n"
+     "            const int32_t* rowk = d + k * ld;\n"
+     "            int64_t dik = rowi[k];\n            if (dik >= O_INF) continue;\n"),
+    ("fw_f64: operand D[k][i] instead of D[i][k]",
+     "double dik = rowi[k];", "double dik = rowk[i];"),
+    ("dijkstra: heap sift-up comparison reversed",
+     "if (!o_less(h, &h->a[c], &h->a[p])) break;", "if (o_less(h, &h->a[c], &h->a[p])) break;"),
+    ("dijkstra: relaxation forgets the distance so far (int)",
+     "int64_t nd = di[u] + g->wi[e];", "int64_t nd = g->wi[e];"),
+    ("dijkstra: relaxation forgets the distance so far (float)",
+     "double nd = df[u] + g->wf[e];", "double nd = g->wf[e];"),
+    ("dijkstra: float weight read transposed",
+     "g->wf[e] = (double)wf32[i * ld + j];", "g->wf[e] = (double)wf32[j * ld + i];"),
+]
+
+
+def _build_mutant(tmp_path, idx, old, new):
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"planted mistake {idx} no longer matches the oracle source"
+    src = src.replace(old, new, 1)
+    c = tmp_path / f"mutant{idx}.c"
+    c.write_text(src)
+    so = tmp_path / f"libmutant{idx}.so"
+    oracle.compile_source(str(c), str(so))
+    return oracle.Oracle(oracle.bind(str(so)))
+
+
+@pytest.mark.parametrize("idx", range(len(MUTANTS)), ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, idx):
+    desc, old, new = MUTANTS[idx]
+    orc = _build_mutant(tmp_path, idx, old, new)
+    bad = pins.run_all(orc)
+    assert bad, f"no pin caught the planted mistake: {desc}"
