@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Benchmark of libapsp (blocked Floyd-Warshall APSP) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload ba16384]
+
+One step = one full solve (all rounds of phases 1-3) of the workload's n x n
+matrix, already resident in device memory.  Before each step the input is
+restored from a pristine device copy; the restore is not timed.  The matrix
+(1 GiB at n = 16384) is far larger than L2, so no flush is needed.  Metric:
+relaxations per second, n^3 / solve time.
+
+Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank solves
+its own replica (replicas only: the path has no exchange step on one GPU).
+The throughput is summed over ranks and the time is the maximum over ranks.
+
+--impl reference times the CPU oracle (the untiled triple loop, all host
+cores) on a bounded sample of the same workload: the first few k-steps of
+Floyd-Warshall on the full matrix.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import graphgen  # noqa: E402
+
+METRIC = "APSP relaxations/sec (n³/time) and % of GB300 INT32 add-min peak, 1 GPU"
+UNIT = "relaxations/s"
+TB = 128
+NOMINAL_INT32_LANES = 128  # INT32 lanes per SM per clock (nominal, one add-min per lane)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ba16384", choices=sorted(graphgen.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(f"/tmp/apsp_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.out is not None:
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return None
+        rows = []
+        try:
+            with open(self.out.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+            os.unlink(self.out.name)
+        except OSError:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ CPU side
+
+def cpu_oracle_sample(w: np.ndarray, target_s: float = 12.0, cap_steps: int = 4096):
+    """Time the oracle's untiled Floyd-Warshall (all host cores) on the first
+    k-steps of the full matrix.  Returns (relax/s, steps, seconds, threads)."""
+    import oracle
+
+    thr = oracle.default_threads()
+    d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
+    n = d.shape[0]
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    orc.fw_i32_steps(d, 0, 1, threads=thr)
+    one = max(time.perf_counter() - t0, 1e-4)
+    steps = int(max(1, min(cap_steps, n - 1, target_s / one)))
+    t0 = time.perf_counter()
+    orc.fw_i32_steps(d, 1, 1 + steps, threads=thr)
+    dt = time.perf_counter() - t0
+    return steps * float(n) * n / dt, steps, dt, thr
+
+
+def reference_arm(args, rank):
+    """--impl reference: the oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+
+    w = graphgen.make(args.workload)
+    n = w.shape[0]
+    d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
+    orc = oracle.default()
+    thr = oracle.default_threads()
+    # size one step to about 2-3 s so that W + K steps finish in a few minutes
+    t0 = time.perf_counter()
+    orc.fw_i32_steps(d, 0, 1, threads=thr)
+    one = max(time.perf_counter() - t0, 1e-4)
+    ks = int(max(1, min(n // max(1, args.steps + args.warmup), 2.5 / one)))
+    k = 1
+    for _ in range(args.warmup):
+        kk = min(n, k + ks)
+        orc.fw_i32_steps(d, k, kk, threads=thr)
+        k = kk % n
+    times = []
+    for _ in range(args.steps):
+        kk = min(n, k + ks)
+        t0 = time.perf_counter()
+        orc.fw_i32_steps(d, k, kk, threads=thr)
+        times.append(time.perf_counter() - t0)
+        k = kk % n
+    tot = sum(times)
+    value = args.steps * ks * float(n) * n / tot
+    sample = (f"{ks} Floyd-Warshall k-steps of the untiled triple loop on the full "
+              f"n={n} {args.workload} matrix per step ({ks * n * n:.3g} relaxations)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload),
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU side
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("fw_kernels.cuh", "fw_launch_impl.cuh"):
+        with open(os.path.join(ROOT, "min_graph_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def phase3_traffic(n: int):
+    """DRAM bytes per phase-3 launch from the committed ncu summary, scaled by
+    tiles; None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "phase3_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    if rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    nb = -(-n // TB)
+    return rec["dram_bytes_per_tile"] * (nb - 1) ** 2
+
+
+def ours(args, rank, world, local):
+    import torch
+
+    import min_graph_gb300 as apsp
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    cfg = graphgen.CONFIGS[args.workload]
+    n = cfg["n"]
+    w = graphgen.make(args.workload)
+    dtype = torch.int32 if w.dtype == np.int32 else torch.float32
+    pristine = torch.from_numpy(w).to(dev)
+    work = torch.empty_like(pristine)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_solve():
+        apsp.solve(work, stream=stream)
+
+    for _ in range(args.warmup):
+        work.copy_(pristine)
+        step_solve()
+    apsp.stream_check(stream)
+
+    nb = -(-n // TB)
+    launches_per_solve = nb + (2 * nb if nb > 1 else 0)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    apsp.phase_timing_read()
+    barrier()
+    with ClockSampler(local) as clocks:
+        apsp.phase_timing_enable(True)
+        for k in range(args.steps):
+            work.copy_(pristine)  # restore the input (outside the events)
+            starts[k].record(stream)
+            step_solve()
+            ends[k].record(stream)
+        barrier()
+        apsp.phase_timing_enable(False)
+    apsp.stream_check(stream)
+    phase_ms, phase_cnt = apsp.phase_timing_read()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    relax_per_step = float(n) ** 3
+    value = world * args.steps * relax_per_step / (total_ms * 1e-3)
+
+    # correctness spot check of the timed result: four oracle rows
+    check = None
+    if rank == 0:
+        import oracle
+
+        src = np.array([0, n // 3, (2 * n) // 3, n - 1], dtype=np.int32)
+        got = work[src.tolist(), :].cpu().numpy()
+        if dtype == torch.int32:
+            ref = oracle.dijkstra_i32(w, src)
+            check = bool(np.array_equal(got, ref))
+        else:
+            ref = oracle.dijkstra_f32(w, src)
+            fin = np.isfinite(ref)
+            check = bool(np.array_equal(np.isfinite(got), fin) and
+                         np.all(np.abs(got[fin] - ref[fin]) <= 1e-5 * np.abs(ref[fin])))
+
+    # end to end through the host-buffer C-ABI call (pinned memory)
+    e2e = None
+    if not args.no_e2e:
+        host_src = torch.from_numpy(w)
+        pinned = torch.empty_like(host_src).pin_memory()
+        pinned.copy_(host_src)
+        apsp.solve_host(pinned)  # warm-up (allocates the staging buffer)
+        e2e_times = []
+        for _ in range(args.steps):
+            pinned.copy_(host_src)
+            barrier()
+            t0 = time.perf_counter()
+            apsp.solve_host(pinned)
+            e2e_times.append(time.perf_counter() - t0)
+        e2e_total = sum(e2e_times)
+        if dist is not None:
+            t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_total = float(t.item())
+        nbytes = n * n * w.itemsize
+        e2e = {"value": world * args.steps * relax_per_step / e2e_total, "unit": UNIT,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+               "ms_per_step": e2e_total / args.steps * 1e3}
+
+    # roofline of the dominant kernel (phase 3): algorithmic relaxations per
+    # launch / average launch time, against SMs x 128 lanes x clock
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    pk = peaks()
+    clk = clocks.summary()
+    f_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
+    f_load = (clk or {}).get("sm_mhz")
+    p3_launches = phase_cnt[2]
+    p3_ms = phase_ms[2] / p3_launches if p3_launches else None
+    p3_relax = float(nb - 1) ** 2 * TB ** 3 if nb > 1 else 0.0
+    ops_per_relax = 1 if dtype == torch.int32 else 2
+    peak_tops = sms * NOMINAL_INT32_LANES * f_max * 1e6 / ops_per_relax / 1e12
+    roof = None
+    if p3_ms:
+        achieved = p3_relax / (p3_ms * 1e-3) / 1e12
+        traffic = phase3_traffic(n)
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Trelax/s",
+                "frac": achieved / peak_tops, "traffic": traffic,
+                "kernel": "fw_phase3_minplus", "peak_basis":
+                    f"{sms} SMs x {NOMINAL_INT32_LANES} INT32 lanes x {f_max:.0f} MHz"
+                    + (" / 2 ops per fp32 relaxation" if ops_per_relax == 2 else ""),
+                "frac_at_load_clock": (achieved / (peak_tops * f_load / f_max)) if f_load else None,
+                "avg_launch_ms": p3_ms, "launches": p3_launches,
+                "phase_share": [m / sum(phase_ms) for m in phase_ms] if sum(phase_ms) > 0 else None}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and dtype == torch.int32:
+        v, ksteps, secs, thr = cpu_oracle_sample(w)
+        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"first {ksteps} k-steps of the untiled Floyd-Warshall triple loop on the "
+                         f"full n={n} matrix ({secs:.1f} s, {thr} threads)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32" if dtype == torch.int32 else "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload),
+                       "l2": f"input {n * n * w.itemsize / 2**30:.2f} GiB > L2; restored from a device "
+                             "copy before each step, outside the timed events",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "pct_int32_addmin_peak": (roof["frac"] * 100) if roof else None,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * launches_per_solve,
+            "clocks": clk, "check_rows_vs_oracle": check,
+            "step_ms": step_ms,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,412 @@
+// C-ABI of libapsp: argument checks, the per-device workspace, the round
+// driver and the precondition validator.
+//
+// Round driver (blocked Floyd-Warshall thesis page, 1library.co excerpt,
+// section 4.6): the primary tile walks down the diagonal, one round per
+// tile, and each round runs phase 1, phase 2 and phase 3 as separate kernels
+// in stream order.  The matrix never leaves device memory (section 4.6.1:
+// the whole graph lives in global memory).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/apsp.h"
+#include "fw_launch.h"
+
+namespace {
+
+constexpr int kTB = APSP_TILE;
+thread_local int g_last_cuda_error = 0;
+
+apsp_status_t cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return APSP_ECUDA;
+}
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    bool init_i32 = false, init_f32 = false;
+    void* ws = nullptr;          // workspace: panels + primary tiles
+    size_t ws_bytes = 0;
+    void* stage = nullptr;       // staging matrix for the host-buffer entry points
+    size_t stage_bytes = 0;
+    cudaEvent_t done = nullptr;  // end of the last solve that used ws
+};
+
+std::mutex g_mu;
+std::vector<DeviceState> g_dev;
+
+// Phase timing (profiling hook).
+struct Timing {
+    bool enabled = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[3];
+    std::vector<cudaEvent_t> pool;
+    double ms[3] = {0, 0, 0};
+    long long launches[3] = {0, 0, 0};
+};
+Timing g_timing;
+
+cudaEvent_t timing_event() {
+    if (!g_timing.pool.empty()) {
+        cudaEvent_t e = g_timing.pool.back();
+        g_timing.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+apsp_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+    DeviceState& st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        st.supported = (major == 10 && minor == 3);
+        st.probed = true;
+    }
+    if (!st.supported) return APSP_EUNSUPPORTED;
+    if (!st.done) {
+        e = cudaEventCreateWithFlags(&st.done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *out = &st;
+    return APSP_OK;
+}
+
+// Grow-only device buffer; waits for the last solve before freeing.
+apsp_status_t ensure_buffer(DeviceState& st, void** buf, size_t* have, size_t need) {
+    if (*have >= need) return APSP_OK;
+    if (*buf) {
+        cudaError_t e = cudaEventSynchronize(st.done);
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
+    }
+    cudaError_t e = cudaMalloc(buf, need);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free allocation error
+        *buf = nullptr;
+        g_last_cuda_error = (int)e;
+        return APSP_ENOMEM;
+    }
+    *have = need;
+    return APSP_OK;
+}
+
+bool args_ok(const void* p, int n, int ld) {
+    if (n < 0 || n > APSP_MAX_N || ld < n) return false;
+    if (n > 0 && p == nullptr) return false;
+    return true;
+}
+
+template <typename T>
+cudaError_t init_kernels(DeviceState& st);
+template <>
+cudaError_t init_kernels<int32_t>(DeviceState& st) {
+    if (st.init_i32) return cudaSuccess;
+    cudaError_t e = apsp::kernels_init<int32_t>();
+    st.init_i32 = (e == cudaSuccess);
+    return e;
+}
+template <>
+cudaError_t init_kernels<float>(DeviceState& st) {
+    if (st.init_f32) return cudaSuccess;
+    cudaError_t e = apsp::kernels_init<float>();
+    st.init_f32 = (e == cudaSuccess);
+    return e;
+}
+
+template <typename T>
+cudaError_t launch_phase(int phase, const apsp::RoundArgs& a, int r, cudaStream_t s) {
+    switch (phase) {
+        case 0: return apsp::launch_phase1<T>(a, r, s);
+        case 1: return apsp::launch_phase2<T>(a, r, s);
+        default: return apsp::launch_phase3<T>(a, r, s);
+    }
+}
+
+// Enqueue a full solve.  Caller holds g_mu.
+template <typename T>
+apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st) {
+    cudaError_t e = init_kernels<T>(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int nb = (n + kTB - 1) / kTB;
+    const int npad = nb * kTB;
+    apsp_status_t rc = ensure_buffer(st, &st.ws, &st.ws_bytes, apsp::workspace_bytes(n));
+    if (rc != APSP_OK) return rc;
+
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const bool capturing = (cap != cudaStreamCaptureStatusNone);
+    if (!capturing) {
+        e = cudaStreamWaitEvent(s, st.done, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+
+    char* w = static_cast<char*>(st.ws);
+    apsp::RoundArgs a;
+    a.d = d;
+    a.ld = ld;
+    a.n = n;
+    a.nb = nb;
+    a.vec = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ld % 4) == 0) ? 1 : 0;
+    a.npad = npad;
+    a.rowp = w;
+    a.colpT = w + (size_t)kTB * npad * sizeof(T);
+    a.prim = w + 2 * (size_t)kTB * npad * sizeof(T);
+    a.primT = w + 2 * (size_t)kTB * npad * sizeof(T) + (size_t)kTB * kTB * sizeof(T);
+
+    const bool timed = g_timing.enabled && !capturing;
+    for (int r = 0; r < nb; ++r) {
+        for (int phase = 0; phase < 3; ++phase) {
+            if (phase > 0 && nb < 2) break;
+            cudaEvent_t e0 = nullptr, e1 = nullptr;
+            if (timed) {
+                e0 = timing_event();
+                e1 = timing_event();
+                if (e0) cudaEventRecord(e0, s);
+            }
+            e = launch_phase<T>(phase, a, r, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (timed && e0 && e1) {
+                cudaEventRecord(e1, s);
+                g_timing.pending[phase].emplace_back(e0, e1);
+            }
+        }
+    }
+    if (!capturing) {
+        e = cudaEventRecord(st.done, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return APSP_OK;
+}
+
+template <typename T>
+apsp_status_t solve_device(T* d, int n, int ld, cudaStream_t s) {
+    if (!args_ok(d, n, ld)) return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    apsp_status_t rc = device_state(&st);
+    if (rc != APSP_OK) return rc;
+    return solve_locked<T>(d, n, ld, s, *st);
+}
+
+template <typename T>
+apsp_status_t solve_host(T* h, int n, int ld, cudaStream_t s) {
+    if (!args_ok(h, n, ld)) return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    apsp_status_t rc = device_state(&st);
+    if (rc != APSP_OK) return rc;
+    const int ldd = (n + 3) & ~3;  // vector-friendly device pitch
+    rc = ensure_buffer(*st, &st->stage, &st->stage_bytes, (size_t)n * ldd * sizeof(T));
+    if (rc != APSP_OK) return rc;
+    T* dd = static_cast<T*>(st->stage);
+    cudaError_t e;
+    if (ld == ldd)
+        e = cudaMemcpyAsync(dd, h, (size_t)n * ld * sizeof(T), cudaMemcpyHostToDevice, s);
+    else
+        e = cudaMemcpy2DAsync(dd, (size_t)ldd * sizeof(T), h, (size_t)ld * sizeof(T),
+                              (size_t)n * sizeof(T), n, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rc = solve_locked<T>(dd, n, ldd, s, *st);
+    if (rc != APSP_OK) return rc;
+    if (ld == ldd)
+        e = cudaMemcpyAsync(h, dd, (size_t)n * ld * sizeof(T), cudaMemcpyDeviceToHost, s);
+    else
+        e = cudaMemcpy2DAsync(h, (size_t)ld * sizeof(T), dd, (size_t)ldd * sizeof(T),
+                              (size_t)n * sizeof(T), n, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return APSP_OK;
+}
+
+// ------------------------------------------------------------- validator
+
+template <typename T>
+__device__ __forceinline__ int entry_flags(T v, bool diag);
+template <>
+__device__ __forceinline__ int entry_flags<int32_t>(int32_t v, bool diag) {
+    return ((diag && v != 0) ? 1 : 0) | (v < 0 ? 2 : 0);
+}
+template <>
+__device__ __forceinline__ int entry_flags<float>(float v, bool diag) {
+    return ((diag && v != 0.0f) ? 1 : 0) | (v < 0.0f ? 2 : 0) | (isnan(v) ? 4 : 0);
+}
+
+template <typename T>
+__global__ void validate_kernel(const T* __restrict__ d, long long ld, int n, int* flags) {
+    const long long total = (long long)n * n;
+    int f = 0;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long i = idx / n, j = idx - i * n;
+        f |= entry_flags<T>(d[i * ld + j], i == j);
+    }
+    f = __reduce_or_sync(0xffffffffu, f);
+    if (f && (threadIdx.x & 31) == 0) atomicOr(flags, f);
+}
+
+template <typename T>
+apsp_status_t validate(const T* d, int n, int ld, cudaStream_t s, int* flags) {
+    if (!args_ok(d, n, ld) || flags == nullptr) return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState* st = nullptr;
+        apsp_status_t rc = device_state(&st);
+        if (rc != APSP_OK) return rc;
+    }
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long total = (long long)n * n;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    validate_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(d, ld, n, flags);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return APSP_OK;
+}
+
+}  // namespace
+
+namespace apsp {
+size_t workspace_bytes(int n) {
+    const size_t nb = (size_t)(n + kTB - 1) / kTB;
+    const size_t npad = nb * kTB;
+    return (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
+}
+}  // namespace apsp
+
+extern "C" {
+
+apsp_status_t apsp_solve(int32_t* dist, int n, int ld, apsp_stream_t stream) {
+    return solve_device<int32_t>(dist, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_solve_i32(int32_t* dist, int n, int ld, apsp_stream_t stream) {
+    return solve_device<int32_t>(dist, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_solve_f32(float* dist, int n, int ld, apsp_stream_t stream) {
+    return solve_device<float>(dist, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_solve_host_i32(int32_t* host, int n, int ld, apsp_stream_t stream) {
+    return solve_host<int32_t>(host, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_solve_host_f32(float* host, int n, int ld, apsp_stream_t stream) {
+    return solve_host<float>(host, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_validate_i32(const int32_t* dist, int n, int ld, apsp_stream_t stream,
+                                int* flags_dev) {
+    return validate<int32_t>(dist, n, ld, (cudaStream_t)stream, flags_dev);
+}
+
+apsp_status_t apsp_validate_f32(const float* dist, int n, int ld, apsp_stream_t stream,
+                                int* flags_dev) {
+    return validate<float>(dist, n, ld, (cudaStream_t)stream, flags_dev);
+}
+
+apsp_status_t apsp_stream_check(apsp_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return APSP_OK;
+}
+
+int apsp_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* apsp_status_string(apsp_status_t status) {
+    switch (status) {
+        case APSP_OK: return "APSP_OK";
+        case APSP_EINVAL: return "APSP_EINVAL: invalid argument";
+        case APSP_ECUDA: return "APSP_ECUDA: CUDA error";
+        case APSP_ETIMEOUT: return "APSP_ETIMEOUT: device-side wait timed out";
+        case APSP_EUNSUPPORTED: return "APSP_EUNSUPPORTED: device is not sm_103";
+        case APSP_ENOMEM: return "APSP_ENOMEM: device allocation failed";
+    }
+    return "unknown apsp status";
+}
+
+int apsp_version(void) { return 100; }  // 0.1.0
+
+apsp_status_t apsp_release(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    apsp_status_t rc = APSP_OK;
+    for (size_t dev = 0; dev < g_dev.size(); ++dev) {
+        DeviceState& st = g_dev[dev];
+        if (!st.ws && !st.stage && !st.done) continue;
+        if (cudaSetDevice((int)dev) != cudaSuccess) { rc = APSP_ECUDA; continue; }
+        if (st.done) cudaEventSynchronize(st.done);
+        if (st.ws) cudaFree(st.ws);
+        if (st.stage) cudaFree(st.stage);
+        if (st.done) cudaEventDestroy(st.done);
+        st.ws = st.stage = nullptr;
+        st.ws_bytes = st.stage_bytes = 0;
+        st.done = nullptr;
+    }
+    cudaSetDevice(cur);
+    return rc;
+}
+
+apsp_status_t apsp_phase_timing_enable(int enable) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_timing.enabled = (enable != 0);
+    return APSP_OK;
+}
+
+apsp_status_t apsp_phase_timing_read(double ms_out[3], long long launches_out[3]) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    apsp_status_t rc = APSP_OK;
+    for (int p = 0; p < 3; ++p) {
+        for (auto& pr : g_timing.pending[p]) {
+            float ms = 0.f;
+            cudaError_t e = cudaEventSynchronize(pr.second);
+            if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, pr.first, pr.second);
+            if (e != cudaSuccess) {
+                g_last_cuda_error = (int)e;
+                rc = APSP_ECUDA;
+            } else {
+                g_timing.ms[p] += ms;
+                g_timing.launches[p] += 1;
+            }
+            g_timing.pool.push_back(pr.first);
+            g_timing.pool.push_back(pr.second);
+        }
+        g_timing.pending[p].clear();
+        if (ms_out) ms_out[p] = g_timing.ms[p];
+        if (launches_out) launches_out[p] = g_timing.launches[p];
+        g_timing.ms[p] = 0;
+        g_timing.launches[p] = 0;
+    }
+    return rc;
+}
+
+}  // extern "C"

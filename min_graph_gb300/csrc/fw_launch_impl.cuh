@@ -1,0 +1,61 @@
+// Launch wrappers for one element type; included once per type by
+// fw_i32.cu and fw_f32.cu so that the two instantiations compile in parallel.
+#pragma once
+
+#include "fw_kernels.cuh"
+#include "fw_launch.h"
+
+namespace apsp {
+
+template <typename T>
+cudaError_t kernels_init_impl() {
+    cudaError_t e = cudaFuncSetAttribute(fw_phase2_panels<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPhase2Smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fw_phase3_minplus<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kPhase3Smem);
+}
+
+template <typename T>
+cudaError_t launch_phase1_impl(const RoundArgs& a, int r, cudaStream_t s) {
+    fw_phase1_diag<T><<<1, P1_THREADS, 0, s>>>(static_cast<T*>(a.d), a.ld, a.n, r,
+                                               static_cast<T*>(a.prim), static_cast<T*>(a.primT),
+                                               a.vec);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_phase2_impl(const RoundArgs& a, int r, cudaStream_t s) {
+    if (a.nb < 2) return cudaSuccess;
+    fw_phase2_panels<T><<<dim3(a.nb - 1, 2), MM_THREADS, kPhase2Smem, s>>>(
+        static_cast<T*>(a.d), a.ld, a.n, r, static_cast<T*>(a.rowp), static_cast<T*>(a.colpT),
+        static_cast<const T*>(a.prim), static_cast<const T*>(a.primT), a.npad, a.vec);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_phase3_impl(const RoundArgs& a, int r, cudaStream_t s) {
+    if (a.nb < 2) return cudaSuccess;
+    const unsigned tiles = (unsigned)(a.nb - 1) * (unsigned)(a.nb - 1);
+    fw_phase3_minplus<T><<<tiles, MM_THREADS, kPhase3Smem, s>>>(
+        static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, static_cast<const T*>(a.rowp),
+        static_cast<const T*>(a.colpT), a.npad, a.vec);
+    return cudaGetLastError();
+}
+
+}  // namespace apsp
+
+#define APSP_INSTANTIATE_LAUNCHERS(T)                                                            \
+    namespace apsp {                                                                             \
+    template <> cudaError_t kernels_init<T>() { return kernels_init_impl<T>(); }                \
+    template <> cudaError_t launch_phase1<T>(const RoundArgs& a, int r, cudaStream_t s) {        \
+        return launch_phase1_impl<T>(a, r, s);                                                   \
+    }                                                                                            \
+    template <> cudaError_t launch_phase2<T>(const RoundArgs& a, int r, cudaStream_t s) {        \
+        return launch_phase2_impl<T>(a, r, s);                                                   \
+    }                                                                                            \
+    template <> cudaError_t launch_phase3<T>(const RoundArgs& a, int r, cudaStream_t s) {        \
+        return launch_phase3_impl<T>(a, r, s);                                                   \
+    }                                                                                            \
+    }

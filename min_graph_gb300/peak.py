@@ -1,0 +1,46 @@
+"""Binding of libapsp_peak.so: measured issue rate of the relaxation step
+(the compute roofline of the min-plus update).  See include/apsp_peak.h."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_SO = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libapsp_peak.so")
+_lib = None
+
+VARIANTS = {
+    0: "int32 fused add-min (__viaddmin_s32)",
+    1: "int32 add then min",
+    2: "int32 two relaxations per three-input min (__vimin3_s32)",
+    3: "fp32 fminf(acc, a+b)",
+    4: "fp32 fminf(acc, fminf(a0+b0, a1+b1))",
+}
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"{_SO} not built; run `python -m min_graph_gb300.build`")
+        lib = ctypes.CDLL(_SO)
+        lib.apsp_peak_addmin.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_longlong)]
+        lib.apsp_peak_addmin.restype = ctypes.c_int
+        lib.apsp_peak_variants.argtypes = []
+        lib.apsp_peak_variants.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def measure(variant: int, blocks: int, threads: int = 256, iters: int = 4096) -> dict:
+    """Run one variant; returns relaxations per SM-clock per SM, ms, total."""
+    rpc, ms, tot = ctypes.c_double(), ctypes.c_double(), ctypes.c_longlong()
+    rc = _load().apsp_peak_addmin(variant, blocks, threads, iters, ctypes.byref(rpc),
+                                  ctypes.byref(ms), ctypes.byref(tot))
+    if rc != 0:
+        raise RuntimeError(f"apsp_peak_addmin({variant}) failed: {rc}")
+    return {"variant": variant, "what": VARIANTS[variant], "relax_per_clk_sm": rpc.value,
+            "ms": ms.value, "relax": tot.value,
+            "relax_per_s": tot.value / (ms.value * 1e-3) if ms.value > 0 else 0.0}

@@ -1,0 +1,89 @@
+"""The C-ABI boundary on a machine without a GPU: the library builds, loads,
+exports every symbol the headers declare, and rejects bad arguments before
+touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import min_graph_gb300 as apsp
+from min_graph_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libs():
+    return mbuild.build()
+
+
+def declared_functions(header: str):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(apsp_\w+)\s*\(", text)))
+
+
+@pytest.mark.parametrize("header,lib", [("apsp.h", "libapsp.so"), ("apsp_peak.h", "libapsp_peak.so")])
+def test_every_declared_symbol_is_exported(libs, header, lib):
+    names = declared_functions(header)
+    assert names, header
+    so = ctypes.CDLL(libs[lib])
+    missing = [n for n in names if not hasattr(so, n)]
+    assert not missing, f"{lib} lacks {missing}"
+
+
+def test_header_constants_match_binding():
+    text = open(os.path.join(ROOT, "include", "apsp.h")).read()
+    assert re.search(r"#define APSP_INF_I32 0x3FFFFFFF", text)
+    assert apsp.INF_I32 == 0x3FFFFFFF
+    assert f"#define APSP_TILE {apsp.TILE}" in text
+    assert f"#define APSP_MAX_N {apsp.MAX_N}" in text
+
+
+def test_status_strings_and_version(libs):
+    lib = apsp.load()
+    for code in range(6):
+        s = lib.apsp_status_string(code).decode()
+        assert s.startswith("APSP_")
+    assert lib.apsp_status_string(99).decode() == "unknown apsp status"
+    assert apsp.version() == 100
+
+
+def test_bad_arguments_rejected_without_cuda(libs):
+    lib = apsp.load()
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    for fn in (lib.apsp_solve, lib.apsp_solve_i32, lib.apsp_solve_f32,
+               lib.apsp_solve_host_i32, lib.apsp_solve_host_f32):
+        assert fn(None, 5, 5, None) == apsp.EINVAL         # NULL with n > 0
+        assert fn(fake, -1, 5, None) == apsp.EINVAL        # n < 0
+        assert fn(fake, 6, 5, None) == apsp.EINVAL         # ld < n
+        assert fn(fake, apsp.MAX_N + 1, apsp.MAX_N + 1, None) == apsp.EINVAL
+        assert fn(None, 0, 0, None) == apsp.OK              # n = 0 is a no-op
+    for fn in (lib.apsp_validate_i32, lib.apsp_validate_f32):
+        assert fn(fake, 4, 4, None, None) == apsp.EINVAL    # no flags pointer
+        assert fn(fake, 4, 3, None, fake) == apsp.EINVAL
+    assert lib.apsp_phase_timing_enable(0) == apsp.OK
+
+
+def test_python_binding_rejects_non_cuda():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        apsp.solve(torch.zeros(4, 4, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        apsp.solve(torch.zeros(4, 5, dtype=torch.int32))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(apsp, "_lib", None)
+    monkeypatch.setattr(apsp, "_LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        apsp.load()
+
+
+def test_workspace_layout_is_16_byte_aligned():
+    # Panels are TB x npad entries with npad a multiple of the tile, so every
+    # workspace section starts on a 64 KiB boundary.
+    for n in (1, 127, 128, 129, 1000, 32768):
+        npad = -(-n // apsp.TILE) * apsp.TILE
+        assert (apsp.TILE * npad * 4) % 65536 == 0

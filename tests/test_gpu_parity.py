@@ -1,0 +1,220 @@
+"""GPU parity: libapsp on the GPU against the CPU oracle, element by element.
+
+int32 results must be bit-exact; fp32 results must be within 1e-5 relative
+error of the fp64 oracle, with the same +inf pattern and a zero diagonal.
+Small cases span several 128 x 128 tiles and ragged tails; the five standard
+workloads are checked at full size (the matrix in full where the oracle can
+afford it, otherwise on 64 seeded rows and columns from Dijkstra).
+"""
+import numpy as np
+import pytest
+
+import graphgen
+import oracle
+import pins
+from gpu_util import INF, assert_f32_close, assert_i32_exact, gpu_solve, threads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import min_graph_gb300 as apsp  # noqa: E402
+
+SIZES = [1, 2, 3, 15, 16, 17, 100, 127, 128, 129, 255, 256, 257, 300, 520, 1000]
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("p", [0.01, 0.1, 0.6])
+def test_random_int32_exact(n, p):
+    w = graphgen.er_i32(n, p, 1, 1000, seed=1000 + n)
+    got, pad_ok = gpu_solve(w)
+    assert pad_ok
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), f"n={n} p={p}")
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("p", [0.01, 0.1, 0.6])
+def test_random_f32_close(n, p):
+    w = graphgen.er_f32(n, p, seed=2000 + n)
+    got, pad_ok = gpu_solve(w)
+    assert pad_ok
+    assert_f32_close(got, oracle.fw_f64(w, threads=threads()), f"n={n} p={p}")
+
+
+@pytest.mark.parametrize("n,ld,offset", [(300, 307, 0), (300, 312, 0), (257, 260, 1),
+                                         (129, 129, 3), (640, 644, 0), (383, 1000, 5)])
+def test_leading_dimension_alignment_and_pad_untouched(n, ld, offset):
+    """ld > n, ld not a multiple of 4, and a base not 16-byte aligned all give
+    the same result; nothing outside the n x n window is written."""
+    w = graphgen.er_i32(n, 0.05, 1, 500, seed=n + ld)
+    got, pad_ok = gpu_solve(w, ld=ld, offset=offset)
+    assert pad_ok, "library wrote outside the matrix"
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), f"n={n} ld={ld} off={offset}")
+    wf = graphgen.er_f32(n, 0.05, seed=n + ld)
+    gotf, pad_ok = gpu_solve(wf, ld=ld, offset=offset)
+    assert pad_ok
+    assert_f32_close(gotf, oracle.fw_f64(wf, threads=threads()), f"f32 n={n} ld={ld}")
+
+
+def test_entries_above_inf_read_as_inf():
+    rng = np.random.default_rng(5)
+    w = graphgen.er_i32(400, 0.05, 1, 100, seed=9)
+    holes = rng.random((400, 400)) < 0.3
+    np.fill_diagonal(holes, False)
+    big = rng.integers(INF + 1, 2**31 - 1, size=(400, 400), dtype=np.int64).astype(np.int32)
+    w2 = np.where(holes & (w == INF), big, w).astype(np.int32)
+    got, _ = gpu_solve(w2)
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), "clamped inputs")
+    assert got.max() == INF
+
+
+def test_golden_fixtures_on_gpu():
+    for path in pins.golden_files():
+        name, dtype, w, d = pins.load_golden(path)
+        got, _ = gpu_solve(w)
+        if dtype == "int32":
+            assert_i32_exact(got, d, name)
+        else:
+            assert np.array_equal(got.astype(np.float64), d), name
+
+
+def test_closed_forms_on_gpu():
+    rng = np.random.default_rng(77)
+    n = 1000  # directed path, 8 tiles with a ragged tail
+    wts = rng.integers(0, 1000, size=n - 1)
+    w = np.full((n, n), INF, dtype=np.int32)
+    np.fill_diagonal(w, 0)
+    w[np.arange(n - 1), np.arange(1, n)] = wts
+    pref = np.concatenate([[0], np.cumsum(wts)])
+    ref = np.where(np.arange(n)[:, None] <= np.arange(n)[None, :], pref[None, :] - pref[:, None], INF)
+    got, _ = gpu_solve(w)
+    assert_i32_exact(got, ref, "directed path")
+    n = 513  # line metric: D = W
+    x = rng.integers(0, 10**6, size=n)
+    w = np.abs(x[:, None] - x[None, :]).astype(np.int32)
+    got, _ = gpu_solve(w)
+    assert_i32_exact(got, w, "line metric")
+
+
+def test_already_closed_matrix_is_a_fixed_point():
+    w = graphgen.er_i32(700, 0.02, 1, 100, seed=3)
+    once, _ = gpu_solve(w)
+    twice, _ = gpu_solve(once)
+    assert_i32_exact(twice, once, "idempotent")
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_workload_er256_full():
+    w = graphgen.make("er256")
+    got, _ = gpu_solve(w)
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), "er256")
+
+
+def test_workload_er2048_full():
+    w = graphgen.make("er2048")
+    got, _ = gpu_solve(w)
+    ref = oracle.fw_i32(w, threads=threads())
+    assert_i32_exact(got, ref, "er2048")
+
+
+def _sample(n, k, seed):
+    rng = np.random.default_rng(seed)
+    s = np.sort(rng.choice(n, size=k, replace=False)).astype(np.int32)
+    s[0], s[-1] = 0, n - 1  # always include both ends (first and ragged-last tiles)
+    return np.unique(s)
+
+
+def test_workload_er8192_sampled_rows_and_columns():
+    w = graphgen.make("er8192")
+    got, _ = gpu_solve(w)
+    src = _sample(8192, 64, 8192)
+    rows = oracle.dijkstra_i32(w, src, threads=threads())
+    cols = oracle.dijkstra_i32(w, src, reverse=True, threads=threads())
+    assert_i32_exact(got[src, :], rows, "er8192 rows")
+    assert_i32_exact(got[:, src].T, cols, "er8192 columns")
+    assert np.all(np.diag(got) == 0)
+
+
+def test_workload_ba16384_full_matrix():
+    """The bench workload: every entry against all-sources Dijkstra."""
+    w = graphgen.make("ba16384")
+    got, _ = gpu_solve(w)
+    ref = oracle.dijkstra_i32(w, np.arange(16384, dtype=np.int32), threads=threads())
+    assert_i32_exact(got, ref, "ba16384")
+
+
+def test_workload_er32768_f32_sampled_rows():
+    w = graphgen.make("er32768")
+    got, _ = gpu_solve(w)
+    src = _sample(32768, 64, 32768)
+    ref = oracle.dijkstra_f32(w, src, threads=threads())
+    assert_f32_close(got[src, :], ref, "er32768 rows", diag_rows=[(i, int(s)) for i, s in enumerate(src)])
+    refc = oracle.dijkstra_f32(w, src[:16], reverse=True, threads=threads())
+    assert_f32_close(got[:, src[:16]].T, refc, "er32768 columns",
+                     diag_rows=[(i, int(s)) for i, s in enumerate(src[:16])])
+
+
+# ---------------------------------------------------------------- API
+
+def test_host_entry_point_matches_device():
+    for n, ld in ((1000, 1000), (601, 603)):
+        w = graphgen.er_i32(n, 0.03, 1, 100, seed=n)
+        buf = np.full((n, ld), -3, dtype=np.int32)
+        buf[:, :n] = w
+        apsp.solve_host(buf, n=n, ld=ld)
+        assert_i32_exact(buf[:, :n], oracle.fw_i32(w, threads=threads()), f"host n={n}")
+        assert np.all(buf[:, n:] == -3)
+        wf = graphgen.er_f32(n, 0.03, seed=n)
+        pinned = torch.from_numpy(wf.copy()).pin_memory()
+        apsp.solve_host(pinned)
+        assert_f32_close(pinned.numpy(), oracle.fw_f64(wf, threads=threads()), f"host f32 n={n}")
+
+
+def test_validator_flags():
+    w = graphgen.er_i32(300, 0.05, 1, 100, seed=1)
+    t = torch.from_numpy(w).cuda()
+    assert apsp.validate(t) == 0
+    t[5, 5] = 3
+    assert apsp.validate(t) == 1
+    t[7, 9] = -2
+    assert apsp.validate(t) == 3
+    f = torch.from_numpy(graphgen.er_f32(300, 0.05, seed=2)).cuda()
+    assert apsp.validate(f) == 0
+    f[1, 2] = float("nan")
+    assert apsp.validate(f) == 4
+
+
+def test_phase_timing_counts_launches():
+    w = torch.from_numpy(graphgen.er_i32(1000, 0.02, 1, 100, seed=4)).cuda()
+    apsp.phase_timing_read()
+    apsp.phase_timing_enable(True)
+    try:
+        apsp.solve(w)
+        ms, cnt = apsp.phase_timing_read()
+    finally:
+        apsp.phase_timing_enable(False)
+    nb = -(-1000 // apsp.TILE)
+    assert cnt == [nb, nb, nb]
+    assert all(m > 0 for m in ms)
+
+
+def test_two_streams_share_the_workspace_safely():
+    ws = [graphgen.er_i32(900, 0.02, 1, 100, seed=s) for s in (1, 2)]
+    ts = [torch.from_numpy(w).cuda() for w in ws]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for t, s in zip(ts, streams):
+        apsp.solve(t, stream=s)
+    torch.cuda.synchronize()
+    for t, w in zip(ts, ws):
+        assert_i32_exact(t.cpu().numpy(), oracle.fw_i32(w, threads=threads()), "two streams")
+
+
+def test_empty_and_single():
+    got, pad_ok = gpu_solve(np.zeros((1, 1), np.int32))
+    assert pad_ok and got[0, 0] == 0
+    t = torch.zeros((0, 0), dtype=torch.int32, device="cuda")
+    apsp.solve(t)
