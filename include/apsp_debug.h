@@ -1,0 +1,33 @@
+/*
+ * libapsp test hooks.  These exist only to exercise failure detection; a
+ * production caller never needs them.
+ */
+#ifndef APSP_DEBUG_H
+#define APSP_DEBUG_H
+
+#include "apsp.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * apsp_debug_inject_phase3_timeout -- arm a one-shot fault for the next
+ * solve that runs the persistent (TMA) phase 3.  In its first phase-3 launch,
+ * CTA 0's producer skips issuing its first k-slab.  The consumers' bounded
+ * wait for that slab then runs out after `timeout_ns`: they record a timeout
+ * in the device error word and leave, and the producer waits (also bounded)
+ * for its copies still in flight before it leaves.  No fault, trap or
+ * unbounded wait is involved.  The next apsp_stream_check() returns
+ * APSP_ETIMEOUT and clears the word.  The matrix content after such a solve
+ * is undefined.
+ *   timeout_ns  1 .. 2e9 nanoseconds, the bound on each wait in that launch.
+ * Returns APSP_EINVAL for an out-of-range timeout.
+ */
+apsp_status_t apsp_debug_inject_phase3_timeout(unsigned long long timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

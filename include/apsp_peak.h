@@ -14,6 +14,25 @@
  *   variant 2: int32, two relaxations per three-input min (__vimin3_s32)
  *   variant 3: fp32, fminf(acc, a + b)
  *   variant 4: fp32, fminf(acc, fminf(a0 + b0, a1 + b1)), two per step
+ *   variant 5: int32, adds as multiply-add by an opaque 1, three-input
+ *              integer min
+ *   variant 6: int32 adds, fp32 three-input min over the (non-negative)
+ *              bit patterns
+ *   variant 7: int32 adds as multiply-add, fp32 three-input min over the
+ *              bit patterns
+ * Variants 0-7 keep their operands in registers.  The compiler may treat
+ * those operands as loop-invariant and move the additions out of the loop.
+ * Variants 1 and 3-7 then measure the minimum alone, and only variant 0
+ * (fused add-min) measures the whole step.
+ * Variants 8-13 run the library's own tile-product inner loop (mm_core.cuh)
+ * on a 32-deep slab resident in shared memory, so they measure the real
+ * step, loads included ( `threads` is ignored: 256 per block):
+ *   variant 8 / 11:  int32 / fp32 fused core (one k per step)
+ *   variant 9 / 12:  int32 / fp32 min3 core (two adds + three-input min)
+ *   variant 10 / 13: int32 / fp32 packed core (one packed add + three-input
+ *                    min, k-pair interleaved operands)
+ *   variant 14 / 15: the int32 fused / fp32 packed core compiled for two
+ *                    resident blocks per SM (at most 128 registers)
  *
  * Outputs (host pointers, any may be NULL):
  *   relax_per_clk_sm  relaxations per SM clock cycle per SM.  Cycles come

@@ -80,6 +80,8 @@ def load():
         lib.apsp_phase_timing_enable.restype = i32
         lib.apsp_phase_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
         lib.apsp_phase_timing_read.restype = i32
+        lib.apsp_debug_inject_phase3_timeout.argtypes = [ctypes.c_ulonglong]
+        lib.apsp_debug_inject_phase3_timeout.restype = i32
         _lib = lib
         return lib
 
@@ -217,3 +219,10 @@ def phase_timing_read():
     cnt = (ctypes.c_longlong * 3)()
     _check(load().apsp_phase_timing_read(ms, cnt), "apsp_phase_timing_read")
     return list(ms), list(cnt)
+
+
+def debug_inject_phase3_timeout(timeout_ns: int) -> None:
+    """Test hook (include/apsp_debug.h): the next solve that runs the
+    persistent phase 3 skips one k-slab, so a bounded device wait runs out
+    after `timeout_ns` and the next stream_check raises ApspError(ETIMEOUT)."""
+    _check(load().apsp_debug_inject_phase3_timeout(int(timeout_ns)), "apsp_debug_inject_phase3_timeout")

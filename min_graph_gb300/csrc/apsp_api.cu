@@ -6,21 +6,27 @@
 // tile, and each round runs phase 1, phase 2 and phase 3 as separate kernels
 // in stream order.  The matrix never leaves device memory (section 4.6.1:
 // the whole graph lives in global memory).
+#include <cuda.h>
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled (fetched through the runtime)
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
 #include "../../include/apsp.h"
+#include "../../include/apsp_debug.h"
 #include "fw_launch.h"
 
 namespace {
 
 constexpr int kTB = APSP_TILE;
+constexpr size_t kErrBytes = 256;  // device error word at the start of the workspace
 thread_local int g_last_cuda_error = 0;
 
 apsp_status_t cuda_fail(cudaError_t e) {
@@ -31,6 +37,7 @@ apsp_status_t cuda_fail(cudaError_t e) {
 struct DeviceState {
     bool probed = false;
     bool supported = false;
+    int sms = 0;
     bool init_i32 = false, init_f32 = false;
     void* ws = nullptr;          // workspace: panels + primary tiles
     size_t ws_bytes = 0;
@@ -41,6 +48,9 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::vector<DeviceState> g_dev;
+int g_inject = 0;  // test hook, consumed by the next persistent phase-3 launch
+unsigned long long g_inject_timeout_ns = 0;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
 // Phase timing (profiling hook).
 struct Timing {
@@ -76,6 +86,8 @@ apsp_status_t device_state(DeviceState** out) {
         e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (e != cudaSuccess) return cuda_fail(e);
         st.supported = (major == 10 && minor == 3);
+        e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
         st.probed = true;
     }
     if (!st.supported) return APSP_EUNSUPPORTED;
@@ -87,8 +99,11 @@ apsp_status_t device_state(DeviceState** out) {
     return APSP_OK;
 }
 
-// Grow-only device buffer; waits for the last solve before freeing.
-apsp_status_t ensure_buffer(DeviceState& st, void** buf, size_t* have, size_t need) {
+// Grow-only device buffer; waits for the last solve before freeing.  Sets
+// *fresh when it allocated.
+apsp_status_t ensure_buffer(DeviceState& st, void** buf, size_t* have, size_t need,
+                            bool* fresh = nullptr) {
+    if (fresh) *fresh = false;
     if (*have >= need) return APSP_OK;
     if (*buf) {
         cudaError_t e = cudaEventSynchronize(st.done);
@@ -105,7 +120,50 @@ apsp_status_t ensure_buffer(DeviceState& st, void** buf, size_t* have, size_t ne
         return APSP_ENOMEM;
     }
     *have = need;
+    if (fresh) *fresh = true;
     return APSP_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched once through the runtime (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Row-major 2-D tensor map: `rows` x `cols` elements of 4 bytes, row pitch
+// `pitch_bytes` (a multiple of 16), box `box_rows` x `box_cols`, no swizzle.
+// Out-of-bounds parts of a box read as zero; the kernels never store them.
+bool encode_2d(CUtensorMap* m, bool is_float, void* base, unsigned long long cols,
+               unsigned long long rows, unsigned long long pitch_bytes, unsigned box_cols,
+               unsigned box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base,
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// APSP_PHASE3=cpasync forces the one-CTA-per-tile cp.async phase 3 even when
+// the persistent TMA kernel could run (for comparison and testing).
+bool persistent_phase3_allowed() {
+    const char* v = std::getenv("APSP_PHASE3");
+    return !(v && std::strcmp(v, "cpasync") == 0);
 }
 
 bool args_ok(const void* p, int n, int ld) {
@@ -147,8 +205,13 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
     if (e != cudaSuccess) return cuda_fail(e);
     const int nb = (n + kTB - 1) / kTB;
     const int npad = nb * kTB;
-    apsp_status_t rc = ensure_buffer(st, &st.ws, &st.ws_bytes, apsp::workspace_bytes(n));
+    bool fresh = false;
+    apsp_status_t rc = ensure_buffer(st, &st.ws, &st.ws_bytes, apsp::workspace_bytes(n), &fresh);
     if (rc != APSP_OK) return rc;
+    if (fresh) {
+        e = cudaMemsetAsync(st.ws, 0, kErrBytes, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     e = cudaStreamIsCapturing(s, &cap);
@@ -159,6 +222,7 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
         if (e != cudaSuccess) return cuda_fail(e);
     }
 
+    // Workspace layout: [error word, 256 B][rowp][colpT][prim][primT].
     char* w = static_cast<char*>(st.ws);
     apsp::RoundArgs a;
     a.d = d;
@@ -167,10 +231,24 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
     a.nb = nb;
     a.vec = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ld % 4) == 0) ? 1 : 0;
     a.npad = npad;
-    a.rowp = w;
-    a.colpT = w + (size_t)kTB * npad * sizeof(T);
-    a.prim = w + 2 * (size_t)kTB * npad * sizeof(T);
-    a.primT = w + 2 * (size_t)kTB * npad * sizeof(T) + (size_t)kTB * kTB * sizeof(T);
+    a.err = reinterpret_cast<int*>(w);
+    a.rowp = w + kErrBytes;
+    a.colpT = w + kErrBytes + (size_t)kTB * npad * sizeof(T);
+    a.prim = w + kErrBytes + 2 * (size_t)kTB * npad * sizeof(T);
+    a.primT = w + kErrBytes + 2 * (size_t)kTB * npad * sizeof(T) + (size_t)kTB * kTB * sizeof(T);
+    a.sms = st.sms;
+    a.tma = 0;
+    a.inject = 0;
+    a.timeout_ns = kDefaultTimeoutNs;
+    const bool is_float = std::is_same<T, float>::value;
+    if (a.vec && nb > 1 && persistent_phase3_allowed()) {
+        const int ks = apsp::phase3_slab_rows();
+        a.tma = encode_2d(&a.tm_c, is_float, d, n, n, (unsigned long long)ld * sizeof(T), kTB, kTB) &&
+                encode_2d(&a.tm_a, is_float, a.colpT, npad, kTB, (unsigned long long)npad * sizeof(T),
+                          kTB, ks) &&
+                encode_2d(&a.tm_b, is_float, a.rowp, npad, kTB, (unsigned long long)npad * sizeof(T),
+                          kTB, ks);
+    }
 
     const bool timed = g_timing.enabled && !capturing;
     for (int r = 0; r < nb; ++r) {
@@ -182,7 +260,17 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
                 e1 = timing_event();
                 if (e0) cudaEventRecord(e0, s);
             }
+            const bool inject_here = (phase == 2 && g_inject && a.tma);
+            if (inject_here) {
+                a.inject = 1;
+                a.timeout_ns = g_inject_timeout_ns;
+                g_inject = 0;
+            }
             e = launch_phase<T>(phase, a, r, s);
+            if (inject_here) {
+                a.inject = 0;
+                a.timeout_ns = kDefaultTimeoutNs;
+            }
             if (e != cudaSuccess) return cuda_fail(e);
             if (timed && e0 && e1) {
                 cudaEventRecord(e1, s);
@@ -295,7 +383,7 @@ namespace apsp {
 size_t workspace_bytes(int n) {
     const size_t nb = (size_t)(n + kTB - 1) / kTB;
     const size_t npad = nb * kTB;
-    return (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
+    return kErrBytes + (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
 }
 }  // namespace apsp
 
@@ -336,6 +424,20 @@ apsp_status_t apsp_stream_check(apsp_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
+    // Device error word of the current device's workspace: a bounded wait
+    // that ran out recorded itself there.  Read it, then clear it.
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= (int)g_dev.size() || !g_dev[dev].ws) return APSP_OK;
+    DeviceState& st = g_dev[dev];
+    int* errp = static_cast<int*>(st.ws);
+    int flags = 0;
+    e = cudaMemcpy(&flags, errp, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (flags != 0) {
+        cudaMemset(errp, 0, sizeof(int));
+        return APSP_ETIMEOUT;
+    }
     return APSP_OK;
 }
 
@@ -374,6 +476,14 @@ apsp_status_t apsp_release(void) {
     }
     cudaSetDevice(cur);
     return rc;
+}
+
+apsp_status_t apsp_debug_inject_phase3_timeout(unsigned long long timeout_ns) {
+    if (timeout_ns == 0 || timeout_ns > kDefaultTimeoutNs) return APSP_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_inject = 1;
+    g_inject_timeout_ns = timeout_ns;
+    return APSP_OK;
 }
 
 apsp_status_t apsp_phase_timing_enable(int enable) {

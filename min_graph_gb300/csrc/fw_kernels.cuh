@@ -14,28 +14,30 @@
 // the already-closed primary tile.  That gives the same distances: the page's
 // in-place loop over k in K computes exactly this product.
 //
-// Phases 2 and 3 share one register-blocked tile product (mm_slab): 256
+// Phases 2 and 3 share one register-blocked tile product (mm_core.cuh): 256
 // threads, each holding an 8 x 8 block of the 128 x 128 output in registers.
 // The A operand is read from shared memory k-major (As[k][i]) and the B
-// operand row-major (Bs[k][j]), each 4 consecutive entries at a time.  The
-// inner step is the fused integer add-min (__viaddmin_s32), or fminf of an
-// IEEE sum for fp32.
-//
-// Phase 3 reads both panels from a compact workspace copy that phase 2
-// writes (row panel as is, column panel transposed), so its k-slabs are
-// plain contiguous rows that cp.async streams into shared memory.
+// operand row-major (Bs[k][j]), 4 consecutive entries at a time.  The inner
+// step is the fused integer add-min (__viaddmin_s32) for int32, and an IEEE
+// add followed by a minimum for fp32.  Measured on sm_103a, the fused
+// add-min keeps the ALU pipe fully busy at 64 relaxations per clock per SM.
+// The two-k alternatives in mm_core.cuh (integer adds + three-input minimum,
+// packed adds) run slower there, limited by issue and dispatch rather than
+// by the ALU pipe.
 #pragma once
 
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mm_core.cuh"
+#include "tma.cuh"
+
 namespace apsp {
 
-constexpr int TB = 128;            // round block = CTA tile edge
 constexpr int P1_THREADS = 512;    // phase 1: 128 rows x 4 quarters
-constexpr int MM_THREADS = 256;    // phases 2 and 3
-constexpr int KS = 32;             // phase 3 k-slab depth
-constexpr int P3_STAGES = 3;       // phase 3 shared-memory ring
+constexpr int MM_THREADS = 256;    // tile-product threads (8 warps)
+constexpr int KS = 32;             // k-slab depth in phase 3
+constexpr int P3_STAGES = 3;       // cp.async ring depth (fallback phase 3)
 constexpr int P1_QPAD = 36;        // phase 1 row buffer quarter stride (bank spread)
 
 template <typename T> struct Sem;
@@ -44,7 +46,7 @@ template <> struct Sem<int32_t> {
     static constexpr int32_t kInf = 0x3FFFFFFF;
     __device__ static __forceinline__ int32_t inf() { return kInf; }
     __device__ static __forceinline__ int32_t clamp(int32_t x) { return min(x, kInf); }
-    // min(a + b, acc); a, b <= INF so a + b <= 2*INF < 2^31.
+    // min(acc, a + b), one relaxation (fused integer add-min).
     __device__ static __forceinline__ int32_t relax(int32_t acc, int32_t a, int32_t b) {
         return __viaddmin_s32(a, b, acc);
     }
@@ -111,9 +113,8 @@ __device__ __forceinline__ void gstore4(T* __restrict__ D, long long ld, int n, 
     }
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -121,56 +122,8 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Thread layout of the 128 x 128 tile product: 8 warps as 4 (rows) x 2
-// (cols), each warp 32 x 64; inside a warp 4 x 8 lanes, each lane owning
-// rows {rA0..rA0+3, rA1..rA1+3} and cols {cB0..cB0+3, cB1..cB1+3}.  For a
-// fixed k the lanes of a warp read 4 distinct 16-byte A chunks and 8 distinct
-// B chunks, all within one shared-memory row: one wavefront each, no bank
-// conflicts.
-struct MMLayout {
-    int rA0, rA1, cB0, cB1;
-    __device__ __forceinline__ explicit MMLayout(int tid) {
-        const int w = tid >> 5, lane = tid & 31;
-        const int wr = w >> 1, wc = w & 1;
-        const int tr = lane >> 3, tc = lane & 7;
-        rA0 = wr * 32 + tr * 4;
-        rA1 = rA0 + 16;
-        cB0 = wc * 64 + tc * 4;
-        cB1 = cB0 + 32;
-    }
-    __device__ __forceinline__ int row(int ri) const { return ri < 4 ? rA0 + ri : rA1 + (ri - 4); }
-    __device__ __forceinline__ int col(int ci) const { return ci < 4 ? cB0 + ci : cB1 + (ci - 4); }
-};
-
-// acc[i][j] = min(acc[i][j], min_k As[k][i] + Bs[k][j]) over k in [0, KLEN).
-// Fragments for step k+1 are loaded while step k computes (two register
-// sets), which hides shared-memory latency without letting the compiler
-// hoist loads further ahead than the register budget allows.
-template <typename T, int KLEN, int UNROLL>
-__device__ __forceinline__ void mm_slab(T (&acc)[8][8], const T* __restrict__ As,
-                                        const T* __restrict__ Bs, const MMLayout& L) {
-    static_assert(UNROLL % 2 == 0 && KLEN % UNROLL == 0, "even unroll");
-    T a[2][8], b[2][8];
-    vload4(As + L.rA0, a[0]);
-    vload4(As + L.rA1, a[0] + 4);
-    vload4(Bs + L.cB0, b[0]);
-    vload4(Bs + L.cB1, b[0] + 4);
-#pragma unroll UNROLL
-    for (int k = 0; k < KLEN; ++k) {
-        const int cur = k & 1, nxt = cur ^ 1;
-        if (k + 1 < KLEN) {
-            vload4(As + (k + 1) * TB + L.rA0, a[nxt]);
-            vload4(As + (k + 1) * TB + L.rA1, a[nxt] + 4);
-            vload4(Bs + (k + 1) * TB + L.cB0, b[nxt]);
-            vload4(Bs + (k + 1) * TB + L.cB1, b[nxt] + 4);
-        }
-#pragma unroll
-        for (int ri = 0; ri < 8; ++ri)
-#pragma unroll
-            for (int ci = 0; ci < 8; ++ci)
-                acc[ri][ci] = Sem<T>::relax(acc[ri][ci], a[cur][ri], b[cur][ci]);
-    }
-}
+// Tile-product core used by phases 2 and 3 for each element type.
+template <typename T> struct Core { static constexpr int value = kCoreFused; };
 
 // ----------------------------------------------------------------- phase 1
 //
@@ -300,7 +253,7 @@ fw_phase2_panels(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ 
         __syncthreads();
     }
 
-    mm_slab<T, TB, 4>(acc, As, Bs, L);
+    mm_core<T, Core<T>::value, TB>(acc, As, Bs, L);
 
     if (is_row) {
 #pragma unroll
@@ -327,47 +280,52 @@ fw_phase2_panels(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ 
     }
 }
 
-// ----------------------------------------------------------------- phase 3
+// Tile (I, J) of the t-th phase-3 work item in round r: row-major over the
+// (nb-1) x (nb-1) grid of non-primary tiles, skipping row and column r.
+__device__ __forceinline__ void phase3_tile(int t, int nbm1, int r, int& I, int& J) {
+    const int ti = t / nbm1, tj = t - ti * nbm1;
+    I = ti + (ti >= r ? 1 : 0);
+    J = tj + (tj >= r ? 1 : 0);
+}
+
+// ------------------------------------------------- phase 3, cp.async version
 //
 // Every tile (I,J) with I != K and J != K (Algorithm 18 of the thesis page,
 // grid (nb-1)^2 with the primary row and column skipped):
 //   D[I,J] <- min(D[I,J], D[I,K] (x) D[K,J]).
-// The panels are read-only in this phase, so k can go in any order.  The
-// panels come from the workspace (colpT gives As[k][i], rowp gives Bs[k][j])
-// in KS-deep slabs through a P3_STAGES-deep cp.async ring.  The C tile goes
-// straight from global memory into the accumulators, and its load overlaps
-// the first slabs' copies.
+// One CTA per tile.  The panels come from the workspace (colpT gives
+// As[k][i], rowp gives Bs[k][j]) in KS-deep slabs through a cp.async ring.
+// This version serves matrices whose base or leading dimension rules out
+// TMA (not 16-byte aligned); fw_phase3_persistent serves the rest.
 template <typename T>
-__global__ void __launch_bounds__(MM_THREADS, 2)
+__global__ void __launch_bounds__(MM_THREADS, 1)
 fw_phase3_minplus(T* __restrict__ D, long long ld, int n, int r, int nbm1,
                   const T* __restrict__ rowp, const T* __restrict__ colpT, int npad, int vec) {
     extern __shared__ __align__(128) unsigned char p3_smem[];
     T* sm = reinterpret_cast<T*>(p3_smem);
     const int tid = threadIdx.x;
-    const int ti = blockIdx.x / nbm1, tj = blockIdx.x - ti * nbm1;
-    const int I = ti + (ti >= r ? 1 : 0), J = tj + (tj >= r ? 1 : 0);
+    int I, J;
+    phase3_tile(blockIdx.x, nbm1, r, I, J);
     const int row0 = I * TB, col0 = J * TB;
     const MMLayout L(tid);
     constexpr int NSLAB = TB / KS;
     constexpr int SLAB = KS * TB;  // elements per operand slab
 
     // Each thread copies the 16-byte chunks c = tid + m * MM_THREADS of a
-    // slab: row kk = c / 32, column 4 * (c % 32).  Offsets stay 32-bit.
-    const unsigned sm_base = static_cast<unsigned>(__cvta_generic_to_shared(sm));
-    const unsigned my_sm = ((tid >> 5) * TB + (tid & 31) * 4) * 4;
+    // slab: row kk = c / 32, column 4 * (c % 32).
+    const uint32_t sm_base = smem_u32(sm);
+    const uint32_t my_sm = ((tid >> 5) * TB + (tid & 31) * 4) * 4;
     const unsigned my_g = (tid >> 5) * npad + (tid & 31) * 4;
     const unsigned row_step_g = (MM_THREADS / 32) * npad;
     auto issue = [&](int s, int st) {
-        const unsigned sa = sm_base + st * 2 * SLAB * 4 + my_sm;
+        const uint32_t sa = sm_base + st * 2 * SLAB * 4 + my_sm;
         const unsigned g = (unsigned)(s * KS) * npad + my_g;
         const T* ga = colpT + row0 + g;
         const T* gb = rowp + col0 + g;
 #pragma unroll
         for (int m = 0; m < SLAB / 4 / MM_THREADS; ++m) {
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa + m * (MM_THREADS / 32) * TB * 4),
-                         "l"(ga + m * row_step_g) : "memory");
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa + SLAB * 4 + m * (MM_THREADS / 32) * TB * 4),
-                         "l"(gb + m * row_step_g) : "memory");
+            cp_async16(sa + m * (MM_THREADS / 32) * TB * 4, ga + m * row_step_g);
+            cp_async16(sa + SLAB * 4 + m * (MM_THREADS / 32) * TB * 4, gb + m * row_step_g);
         }
         cp_async_commit();
     };
@@ -389,7 +347,7 @@ fw_phase3_minplus(T* __restrict__ D, long long ld, int n, int r, int nbm1,
         __syncthreads();
         if (s + 2 < NSLAB) issue(s + 2, (s + 2) % P3_STAGES);
         const T* As = sm + (s % P3_STAGES) * 2 * SLAB;
-        mm_slab<T, KS, 2>(acc, As, As + SLAB, L);
+        mm_core<T, Core<T>::value, KS>(acc, As, As + SLAB, L);
     }
 
 #pragma unroll
@@ -397,6 +355,144 @@ fw_phase3_minplus(T* __restrict__ D, long long ld, int n, int r, int nbm1,
         const int i = row0 + L.row(ri);
         gstore4(D, ld, n, i, col0 + L.cB0, vec != 0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
         gstore4(D, ld, n, i, col0 + L.cB1, vec != 0, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+    }
+}
+
+// --------------------------------------------- phase 3, persistent TMA version
+//
+// Same update as fw_phase3_minplus, restructured for sm_103a: one CTA per SM
+// walks a static round-robin list of tiles.  A producer warp (one elected
+// thread) streams, by TMA, each tile's C block (128 x 128 of D) into a
+// shared buffer and its panel k-slabs (A from colpT, B from rowp) into a
+// P3P_STAGES-deep ring.  The loads run ahead across tile boundaries, so the
+// next tile's data arrive while the current one computes.  Eight consumer
+// warps own the 128 x 128 accumulator block in registers.  They read C once
+// from shared memory, run the paired-k product over the ring, and store the
+// result straight from registers.  Full/empty mbarriers order the two sides,
+// and every wait is bounded (tma.cuh).
+constexpr int P3P_CONSUMERS = MM_THREADS;
+constexpr int P3P_THREADS = P3P_CONSUMERS + 32;
+constexpr int P3P_STAGES = 4;
+constexpr uint32_t P3P_SLAB_BYTES = KS * TB * 4;             // 16 KiB per operand slab
+constexpr uint32_t P3P_STAGE_BYTES = 2 * P3P_SLAB_BYTES;     // A + B
+constexpr uint32_t P3P_C_BYTES = TB * TB * 4;                // 64 KiB
+constexpr size_t kPhase3PSmem = 1024 + P3P_C_BYTES + (size_t)P3P_STAGES * P3P_STAGE_BYTES + 256;
+
+template <typename T>
+__global__ void __launch_bounds__(P3P_THREADS, 1)
+fw_phase3_persistent(T* __restrict__ D, long long ld, int n, int r, int nbm1, int ntiles,
+                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_a,
+                     const __grid_constant__ CUtensorMap tm_b, int* __restrict__ err,
+                     unsigned long long timeout_ns, int inject) {
+    extern __shared__ unsigned char p3p_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(p3p_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    T* cbuf = reinterpret_cast<T*>(base);
+    unsigned char* ring = base + P3P_C_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + P3P_STAGES * P3P_STAGE_BYTES);
+    const uint32_t bar_full = smem_u32(bars);                   // [P3P_STAGES]
+    const uint32_t bar_empty = bar_full + 8 * P3P_STAGES;       // [P3P_STAGES]
+    const uint32_t bar_cfull = bar_empty + 8 * P3P_STAGES;
+    const uint32_t bar_cempty = bar_cfull + 8;
+    const int tid = threadIdx.x;
+    constexpr int NSLAB = TB / KS;
+
+    if (tid == 0) {
+        for (int s = 0; s < P3P_STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, P3P_CONSUMERS / 32);
+        }
+        mbar_init(bar_cfull, 1);
+        mbar_init(bar_cempty, P3P_CONSUMERS / 32);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (tid >= P3P_CONSUMERS) {
+        // ------------------------------------------------------ producer
+        if (tid != P3P_CONSUMERS) return;
+        tma_prefetch_desc(&tm_c);
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        const uint32_t cdst = smem_u32(cbuf);
+        const uint32_t rdst = smem_u32(ring);
+        uint32_t g = 0;   // slabs issued so far
+        int it = 0;       // tiles whose C load was issued
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            int I, J;
+            phase3_tile(t, nbm1, r, I, J);
+            if (it > 0 && !mbar_wait_bounded(bar_cempty, (it - 1) & 1, err, timeout_ns)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(bar_cfull, P3P_C_BYTES);
+            tma_load_2d(cdst, &tm_c, J * TB, I * TB, bar_cfull);
+            ++it;
+            for (int s = 0; s < NSLAB; ++s) {
+                const uint32_t st = g % P3P_STAGES, use = g / P3P_STAGES;
+                if (use > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1, err, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (inject && g == 0 && blockIdx.x == 0) {
+                    // Test hook: this slab is never issued, so the consumers'
+                    // bounded wait on it must run out (APSP_ETIMEOUT).
+                    ++g;
+                    continue;
+                }
+                const uint32_t dst = rdst + st * P3P_STAGE_BYTES;
+                mbar_arrive_expect_tx(bar_full + 8 * st, P3P_STAGE_BYTES);
+                tma_load_2d(dst, &tm_a, I * TB, s * KS, bar_full + 8 * st);
+                tma_load_2d(dst + P3P_SLAB_BYTES, &tm_b, J * TB, s * KS, bar_full + 8 * st);
+                ++g;
+            }
+        }
+        if (!ok) {
+            // Drain: wait (bounded) for every copy still in flight before the
+            // CTA may exit, so no TMA write lands in freed shared memory.
+            for (uint32_t q = (g > P3P_STAGES ? g - P3P_STAGES : 0); q < g; ++q)
+                mbar_wait_bounded(bar_full + 8 * (q % P3P_STAGES), (q / P3P_STAGES) & 1, err,
+                                  timeout_ns, false);
+            if (it > 0) mbar_wait_bounded(bar_cfull, (it - 1) & 1, err, timeout_ns, false);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const MMLayout L(tid);
+    const int lane = tid & 31;
+    uint32_t g = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        int I, J;
+        phase3_tile(t, nbm1, r, I, J);
+        T acc[8][8];
+        if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
+#pragma unroll
+        for (int ri = 0; ri < 8; ++ri) {
+            vload4(cbuf + L.row(ri) * TB + L.cB0, &acc[ri][0]);
+            vload4(cbuf + L.row(ri) * TB + L.cB1, &acc[ri][4]);
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cempty);
+        for (int s = 0; s < NSLAB; ++s, ++g) {
+            const uint32_t st = g % P3P_STAGES, use = g / P3P_STAGES;
+            if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
+            const T* As = reinterpret_cast<const T*>(ring + st * P3P_STAGE_BYTES);
+            mm_core<T, Core<T>::value, KS>(acc, As, As + KS * TB, L);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+        }
+        const int row0 = I * TB, col0 = J * TB;
+#pragma unroll
+        for (int ri = 0; ri < 8; ++ri) {
+            const int i = row0 + L.row(ri);
+            gstore4(D, ld, n, i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+            gstore4(D, ld, n, i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+        }
     }
 }
 

@@ -2,8 +2,10 @@
 // and the per-type kernel translation units (fw_i32.cu, fw_f32.cu).
 #pragma once
 
-#include <cstdint>
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace apsp {
 
@@ -19,6 +21,14 @@ struct RoundArgs {
     void* prim;     // workspace: closed primary tile, TB x TB
     void* primT;    // workspace: its transpose
     int npad;       // nb * TB
+    int tma;        // 1: the persistent TMA phase 3 may run (tensor maps valid)
+    int sms;        // SM count of the device (persistent grid size)
+    int* err;       // device error word (bounded-wait timeouts)
+    unsigned long long timeout_ns;  // bound on every device-side wait
+    int inject;     // test hook: persistent phase 3 skips one slab (forces a timeout)
+    CUtensorMap tm_c;   // D, n x n, box TB x TB
+    CUtensorMap tm_a;   // colpT, TB x npad, box KS x TB
+    CUtensorMap tm_b;   // rowp,  TB x npad, box KS x TB
 };
 
 // Opt the kernels into their shared-memory sizes on the current device.
@@ -27,7 +37,11 @@ template <typename T> cudaError_t launch_phase1(const RoundArgs& a, int r, cudaS
 template <typename T> cudaError_t launch_phase2(const RoundArgs& a, int r, cudaStream_t s);
 template <typename T> cudaError_t launch_phase3(const RoundArgs& a, int r, cudaStream_t s);
 
-// Bytes of workspace the round driver needs for n vertices.
+// Bytes of workspace the round driver needs for n vertices (panels, primary
+// tiles, and the device error word at the end).
 size_t workspace_bytes(int n);
+
+// k-slab depth of the persistent phase 3 (the panel tensor maps' box height).
+int phase3_slab_rows();
 
 }  // namespace apsp

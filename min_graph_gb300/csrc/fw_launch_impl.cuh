@@ -13,8 +13,11 @@ cudaError_t kernels_init_impl() {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPhase2Smem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(fw_phase3_minplus<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kPhase3Smem);
+    e = cudaFuncSetAttribute(fw_phase3_minplus<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPhase3Smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fw_phase3_persistent<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kPhase3PSmem);
 }
 
 template <typename T>
@@ -38,6 +41,13 @@ template <typename T>
 cudaError_t launch_phase3_impl(const RoundArgs& a, int r, cudaStream_t s) {
     if (a.nb < 2) return cudaSuccess;
     const unsigned tiles = (unsigned)(a.nb - 1) * (unsigned)(a.nb - 1);
+    if (a.tma) {
+        const unsigned grid = tiles < (unsigned)a.sms ? tiles : (unsigned)a.sms;
+        fw_phase3_persistent<T><<<grid, P3P_THREADS, kPhase3PSmem, s>>>(
+            static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, (int)tiles, a.tm_c, a.tm_a, a.tm_b, a.err,
+            a.timeout_ns, a.inject);
+        return cudaGetLastError();
+    }
     fw_phase3_minplus<T><<<tiles, MM_THREADS, kPhase3Smem, s>>>(
         static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, static_cast<const T*>(a.rowp),
         static_cast<const T*>(a.colpT), a.npad, a.vec);

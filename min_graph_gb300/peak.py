@@ -14,6 +14,17 @@ VARIANTS = {
     2: "int32 two relaxations per three-input min (__vimin3_s32)",
     3: "fp32 fminf(acc, a+b)",
     4: "fp32 fminf(acc, fminf(a0+b0, a1+b1))",
+    5: "int32 multiply-add adds, three-input integer min",
+    6: "int32 adds, fp32 three-input min on bit patterns",
+    7: "int32 multiply-add adds, fp32 three-input min on bit patterns",
+    8: "core: int32 fused add-min, one k per step (smem-fed)",
+    9: "core: int32 two adds + three-input min (smem-fed)",
+    10: "core: int32 64-bit packed add + three-input min (smem-fed)",
+    11: "core: fp32 add + min, one k per step (smem-fed)",
+    12: "core: fp32 two adds + three-input min (smem-fed)",
+    13: "core: fp32 add.f32x2 + three-input min (smem-fed)",
+    14: "core: int32 fused, compiled for 2 blocks/SM",
+    15: "core: fp32 add.f32x2 + min3, compiled for 2 blocks/SM",
 }
 
 

@@ -24,7 +24,8 @@ def declared_functions(header: str):
     return sorted(set(re.findall(r"\b(apsp_\w+)\s*\(", text)))
 
 
-@pytest.mark.parametrize("header,lib", [("apsp.h", "libapsp.so"), ("apsp_peak.h", "libapsp_peak.so")])
+@pytest.mark.parametrize("header,lib", [("apsp.h", "libapsp.so"), ("apsp_debug.h", "libapsp.so"),
+                                        ("apsp_peak.h", "libapsp_peak.so")])
 def test_every_declared_symbol_is_exported(libs, header, lib):
     names = declared_functions(header)
     assert names, header
@@ -64,6 +65,8 @@ def test_bad_arguments_rejected_without_cuda(libs):
         assert fn(fake, 4, 4, None, None) == apsp.EINVAL    # no flags pointer
         assert fn(fake, 4, 3, None, fake) == apsp.EINVAL
     assert lib.apsp_phase_timing_enable(0) == apsp.OK
+    assert lib.apsp_debug_inject_phase3_timeout(0) == apsp.EINVAL
+    assert lib.apsp_debug_inject_phase3_timeout(3 * 10**9) == apsp.EINVAL
 
 
 def test_python_binding_rejects_non_cuda():

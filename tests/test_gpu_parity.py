@@ -60,7 +60,7 @@ def test_leading_dimension_alignment_and_pad_untouched(n, ld, offset):
 
 def test_entries_above_inf_read_as_inf():
     rng = np.random.default_rng(5)
-    w = graphgen.er_i32(400, 0.05, 1, 100, seed=9)
+    w = graphgen.er_i32(400, 0.002, 1, 100, seed=9)  # sparse: many unreachable pairs
     holes = rng.random((400, 400)) < 0.3
     np.fill_diagonal(holes, False)
     big = rng.integers(INF + 1, 2**31 - 1, size=(400, 400), dtype=np.int64).astype(np.int32)
@@ -218,3 +218,42 @@ def test_empty_and_single():
     assert pad_ok and got[0, 0] == 0
     t = torch.zeros((0, 0), dtype=torch.int32, device="cuda")
     apsp.solve(t)
+
+
+@pytest.mark.parametrize("n", [129, 300, 1000, 2100])
+def test_both_phase3_kernels_agree(n, monkeypatch):
+    """The persistent TMA phase 3 (default for aligned matrices) and the
+    one-CTA-per-tile cp.async phase 3 give identical results."""
+    w = graphgen.er_i32(n, 0.02, 1, 1000, seed=n + 7)
+    ref = oracle.fw_i32(w, threads=threads())
+    got_p, _ = gpu_solve(w)
+    monkeypatch.setenv("APSP_PHASE3", "cpasync")
+    got_c, _ = gpu_solve(w)
+    monkeypatch.delenv("APSP_PHASE3")
+    assert_i32_exact(got_p, ref, "persistent")
+    assert_i32_exact(got_c, ref, "cp.async")
+    wf = graphgen.er_f32(n, 0.02, seed=n + 8)
+    reff = oracle.fw_f64(wf, threads=threads())
+    gf_p, _ = gpu_solve(wf)
+    monkeypatch.setenv("APSP_PHASE3", "cpasync")
+    gf_c, _ = gpu_solve(wf)
+    monkeypatch.delenv("APSP_PHASE3")
+    assert_f32_close(gf_p, reff, "persistent f32")
+    assert_f32_close(gf_c, reff, "cp.async f32")
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A device-side wait that never completes (the test hook withholds one
+    k-slab) ends after its bound; the host sees APSP_ETIMEOUT and the GPU
+    context stays usable."""
+    w = graphgen.er_i32(600, 0.02, 1, 100, seed=12)
+    t = torch.from_numpy(w).cuda()
+    apsp.stream_check()
+    apsp.debug_inject_phase3_timeout(50_000_000)  # 50 ms
+    apsp.solve(t)
+    with pytest.raises(apsp.ApspError) as ei:
+        apsp.stream_check()
+    assert ei.value.status == apsp.ETIMEOUT
+    apsp.stream_check()  # the error word was cleared
+    got, _ = gpu_solve(w)  # and the next solve is correct
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), "after timeout")
