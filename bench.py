@@ -40,6 +40,7 @@ METRIC = "APSP relaxations/sec (n³/time) and % of GB300 INT32 add-min peak, 1 G
 UNIT = "relaxations/s"
 TB = 128
 NOMINAL_INT32_LANES = 128  # INT32 lanes per SM per clock (nominal, one add-min per lane)
+MEASURED_ADDMIN_PER_CLK = 64  # fused add-min issue rate per SM per clock (profiles/relaxation_issue_rate.md)
 
 
 def parse():
@@ -129,23 +130,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU side
 
-def cpu_oracle_sample(w: np.ndarray, target_s: float = 12.0, cap_steps: int = 4096):
+def cpu_oracle_sample(w: np.ndarray, target_s: float = 12.0, chunk: int = 16):
     """Time the oracle's untiled Floyd-Warshall (all host cores) on the first
-    k-steps of the full matrix.  Returns (relax/s, steps, seconds, threads)."""
+    k-steps of the full matrix, in chunks of `chunk` steps until about
+    target_s seconds have passed.  Returns (relax/s, steps, seconds, threads)."""
     import oracle
 
     thr = oracle.default_threads()
     d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
     n = d.shape[0]
     orc = oracle.default()
-    t0 = time.perf_counter()
-    orc.fw_i32_steps(d, 0, 1, threads=thr)
-    one = max(time.perf_counter() - t0, 1e-4)
-    steps = int(max(1, min(cap_steps, n - 1, target_s / one)))
-    t0 = time.perf_counter()
-    orc.fw_i32_steps(d, 1, 1 + steps, threads=thr)
-    dt = time.perf_counter() - t0
-    return steps * float(n) * n / dt, steps, dt, thr
+    k, dt = 0, 0.0
+    while dt < target_s and k < n:
+        kk = min(n, k + chunk)
+        t0 = time.perf_counter()
+        orc.fw_i32_steps(d, k, kk, threads=thr)
+        dt += time.perf_counter() - t0
+        k = kk
+    return k * float(n) * n / dt, k, dt, thr
 
 
 def reference_arm(args, rank):
@@ -159,27 +161,28 @@ def reference_arm(args, rank):
     d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
     orc = oracle.default()
     thr = oracle.default_threads()
-    # size one step to about 2-3 s so that W + K steps finish in a few minutes
-    t0 = time.perf_counter()
-    orc.fw_i32_steps(d, 0, 1, threads=thr)
-    one = max(time.perf_counter() - t0, 1e-4)
-    ks = int(max(1, min(n // max(1, args.steps + args.warmup), 2.5 / one)))
-    k = 1
-    for _ in range(args.warmup):
-        kk = min(n, k + ks)
-        orc.fw_i32_steps(d, k, kk, threads=thr)
-        k = kk % n
+    # Each step runs chunks of k-steps (continuing, wrapping around n) until
+    # about 2.5 s have passed, so that W + K steps finish in a few minutes.
+    chunk, k = 8, 0
+    relax = []
     times = []
-    for _ in range(args.steps):
-        kk = min(n, k + ks)
-        t0 = time.perf_counter()
-        orc.fw_i32_steps(d, k, kk, threads=thr)
-        times.append(time.perf_counter() - t0)
-        k = kk % n
+    for step in range(args.warmup + args.steps):
+        dt, done = 0.0, 0
+        while dt < 2.5:
+            kk = min(n, k + chunk)
+            t0 = time.perf_counter()
+            orc.fw_i32_steps(d, k, kk, threads=thr)
+            dt += time.perf_counter() - t0
+            done += kk - k
+            k = kk % n
+        if step >= args.warmup:
+            times.append(dt)
+            relax.append(done * float(n) * n)
     tot = sum(times)
-    value = args.steps * ks * float(n) * n / tot
-    sample = (f"{ks} Floyd-Warshall k-steps of the untiled triple loop on the full "
-              f"n={n} {args.workload} matrix per step ({ks * n * n:.3g} relaxations)")
+    value = sum(relax) / tot
+    ks = int(round(sum(relax) / len(relax) / (float(n) * n)))
+    sample = (f"about {ks} Floyd-Warshall k-steps of the untiled triple loop on the full "
+              f"n={n} {args.workload} matrix per step (~2.5 s, {thr} threads)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
@@ -197,7 +200,7 @@ def reference_arm(args, rank):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("fw_kernels.cuh", "fw_launch_impl.cuh"):
+    for f in ("fw_kernels.cuh", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"):
         with open(os.path.join(ROOT, "min_graph_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -206,7 +209,7 @@ def kernel_source_hash():
 def phase3_traffic(n: int):
     """DRAM bytes per phase-3 launch from the committed ncu summary, scaled by
     tiles; None when the kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "phase3_traffic.json")
+    path = os.path.join(ROOT, "profiles", "fw_phase3_persistent_er8192_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -215,7 +218,7 @@ def phase3_traffic(n: int):
     if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
     nb = -(-n // TB)
-    return rec["dram_bytes_per_tile"] * (nb - 1) ** 2
+    return rec["dram_bytes_per_tile"] * (nb - 1) ** 2 / 1e9  # GB per launch
 
 
 def ours(args, rank, world, local):
@@ -337,9 +340,15 @@ def ours(args, rank, world, local):
     if p3_ms:
         achieved = p3_relax / (p3_ms * 1e-3) / 1e12
         traffic = phase3_traffic(n)
+        measured_tops = sms * MEASURED_ADDMIN_PER_CLK * f_max * 1e6 / 1e12
+        kernel = ("fw_phase3_minplus" if os.environ.get("APSP_PHASE3") == "cpasync"
+                  else "fw_phase3_persistent")
         roof = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Trelax/s",
                 "frac": achieved / peak_tops, "traffic": traffic,
-                "kernel": "fw_phase3_minplus", "peak_basis":
+                "traffic_unit": "GB per launch (DRAM read + write, scaled from the committed ncu capture)",
+                "peak_measured_addmin": measured_tops,
+                "frac_of_measured_addmin": achieved / measured_tops,
+                "kernel": kernel, "peak_basis":
                     f"{sms} SMs x {NOMINAL_INT32_LANES} INT32 lanes x {f_max:.0f} MHz"
                     + (" / 2 ops per fp32 relaxation" if ops_per_relax == 2 else ""),
                 "frac_at_load_clock": (achieved / (peak_tops * f_load / f_max)) if f_load else None,
