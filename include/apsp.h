@@ -133,6 +133,39 @@ int apsp_version(void);
 apsp_status_t apsp_release(void);
 
 /*
+ * apsp_solve_noalloc -- the int32 solve of apsp_solve for callers that may
+ * not allocate device memory.  The pages have no counterpart to this entry
+ * point: it exists for callers whose GPU memory is owned by another
+ * allocator (a framework's caching pool, or a process held to a fixed memory
+ * budget), or that run where an allocation, which can synchronise the whole
+ * device, is not allowed.
+ *
+ * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).  Its workspace is a fixed scratch array of
+ * APSP_NOALLOC_SCRATCH_BYTES (about 8.1 MiB) in the library's device image.
+ * Every GPU that loads the library holds that array until the process exits.
+ *   dist, n, ld, stream  as for apsp_solve, with n <= APSP_NOALLOC_MAX_N.
+ *                        A larger n returns APSP_EINVAL before any work.
+ *   err_dev              optional device pointer to one int.  After the solve
+ *                        (in stream order) it receives the device error
+ *                        word: 0, or APSP's timeout flag if a bounded
+ *                        device-side wait ran out (the result is then
+ *                        undefined).  NULL skips the copy.
+ * Set-up: the first call on each device does a one-time set-up with that
+ * device current.  It looks up the scratch array's device address
+ * (cudaGetSymbolAddress) and sets the kernels' shared-memory limits.  Make
+ * that first call before any stream capture.
+ * Sharing: all calls share the one array, which keeps the last call's
+ * contents; each call clears what must start at zero.  Calls whose work
+ * overlaps on the GPU (on different streams, or from different host
+ * threads without ordering) race on the array and give wrong results.  Order
+ * them, e.g. on one stream.
+ */
+#define APSP_NOALLOC_MAX_N 8192
+#define APSP_NOALLOC_SCRATCH_BYTES 8519936 /* 256 + (2*128*8192 + 2*128*128) * 4 */
+apsp_status_t apsp_solve_noalloc(int32_t* dist, int n, int ld, apsp_stream_t stream, int* err_dev);
+
+/*
  * Phase timing, for profiling.  While it is enabled, each solve records CUDA
  * events on its stream around every phase launch.  apsp_phase_timing_read
  * waits for those events and returns, per phase (index 0, 1, 2 = phase 1, 2,
