@@ -33,6 +33,10 @@
  *                    min, k-pair interleaved operands)
  *   variant 14 / 15: the int32 fused / fp32 packed core compiled for two
  *                    resident blocks per SM (at most 128 registers)
+ *   variant 16 / 17: int32 mixed core, 2 / 3 of 8 accumulator rows on the
+ *                    fused add-min, the rest on adds + three-input min
+ *   variant 18 / 19 / 20: the same with 2 / 3 / 4 fused rows, the adds
+ *                    written as multiply-adds by an opaque 1 (FMA pipe)
  *
  * Outputs (host pointers, any may be NULL):
  *   relax_per_clk_sm  relaxations per SM clock cycle per SM.  Cycles come

@@ -40,6 +40,13 @@ constexpr int TB = 128;  // tile edge
 constexpr int kCoreFused = 0;
 constexpr int kCoreMin3 = 1;
 constexpr int kCorePacked = 2;
+// Mixed int32 cores: the first R of the 8 accumulator rows take the fused
+// add-min (ALU pipe only); the other rows take two adds + a three-input
+// minimum, which moves the adds to the FMA pipe.  kCoreMixAdd + R lets the
+// compiler place the adds.  kCoreMixMad + R writes each add as a multiply-add
+// by an opaque 1, which runs on the FMA pipe.
+constexpr int kCoreMixAdd = 16;
+constexpr int kCoreMixMad = 32;
 
 // Thread layout of the 128 x 128 tile product: 8 warps as 4 (rows) x 2
 // (cols), each warp 32 x 64; inside a warp 4 x 8 lanes, each lane owning
@@ -107,6 +114,14 @@ template <> struct CoreOps<float> {
         return min3_f32(acc, __uint_as_float((unsigned)s), __uint_as_float((unsigned)(s >> 32)));
     }
 };
+
+// a + b as a multiply-add by `one` (== 1 at run time, unknown to the
+// compiler), so the sum is formed on the FMA pipe.
+__device__ __forceinline__ int32_t add_on_fma(int32_t a, int32_t b, int32_t one) {
+    int32_t d;
+    asm("mad.lo.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(one), "r"(b));
+    return d;
+}
 
 // ------------------------------------------------------------ fragment loads
 
@@ -183,12 +198,49 @@ __device__ __forceinline__ void step2p(T (&acc)[8][8], const unsigned long long*
         for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = CoreOps<T>::relax2p(acc[ri][ci], pa[ri], pb[ci]);
 }
 
-// acc = min(acc, A (x) B) over k in [0, KLEN).  As/Bs: k-major for the fused
-// and min3 cores, k-pair interleaved for the packed core.
+template <int R, bool MAD>
+__device__ __forceinline__ void step_mix(int32_t (&acc)[8][8], const int32_t* a0, const int32_t* b0,
+                                         const int32_t* a1, const int32_t* b1, int32_t one) {
+#pragma unroll
+    for (int ri = 0; ri < 8; ++ri)
+#pragma unroll
+        for (int ci = 0; ci < 8; ++ci) {
+            if (ri < R) {
+                acc[ri][ci] = __viaddmin_s32(a1[ri], b1[ci], __viaddmin_s32(a0[ri], b0[ci], acc[ri][ci]));
+            } else {
+                const int32_t s0 = MAD ? add_on_fma(a0[ri], b0[ci], one) : a0[ri] + b0[ci];
+                const int32_t s1 = MAD ? add_on_fma(a1[ri], b1[ci], one) : a1[ri] + b1[ci];
+                acc[ri][ci] = __float_as_int(
+                    min3_f32(__int_as_float(acc[ri][ci]), __int_as_float(s0), __int_as_float(s1)));
+            }
+        }
+}
+
+// acc = min(acc, A (x) B) over k in [0, KLEN).  As/Bs: k-major for the fused,
+// min3 and mixed cores, k-pair interleaved for the packed core.  `one` must
+// be 1 (used by the kCoreMixMad cores only).
 template <typename T, int CORE, int KLEN>
 __device__ __forceinline__ void mm_core(T (&acc)[8][8], const T* __restrict__ As,
-                                        const T* __restrict__ Bs, const MMLayout& L) {
-    if constexpr (CORE == kCoreFused) {
+                                        const T* __restrict__ Bs, const MMLayout& L, int one = 1) {
+    if constexpr (CORE >= kCoreMixAdd) {
+        static_assert(sizeof(T) == 4 && KLEN % 4 == 0, "mixed cores are int32, k-length % 4 == 0");
+        constexpr int R = CORE & 15;
+        constexpr bool MAD = CORE >= kCoreMixMad;
+        T xa0[8], xb0[8], xa1[8], xb1[8], ya0[8], yb0[8], ya1[8], yb1[8];
+        frag_k(As, Bs, 0, L, xa0, xb0);
+        frag_k(As, Bs, 1, L, xa1, xb1);
+#pragma unroll 1
+        for (int k = 0; k < KLEN; k += 4) {
+            frag_k(As, Bs, k + 2, L, ya0, yb0);
+            frag_k(As, Bs, k + 3, L, ya1, yb1);
+            step_mix<R, MAD>(acc, xa0, xb0, xa1, xb1, one);
+            if (k + 4 < KLEN) {
+                frag_k(As, Bs, k + 4, L, xa0, xb0);
+                frag_k(As, Bs, k + 5, L, xa1, xb1);
+            }
+            step_mix<R, MAD>(acc, ya0, yb0, ya1, yb1, one);
+        }
+    } else if constexpr (CORE == kCoreFused) {
         static_assert(KLEN % 2 == 0, "even k-length");
         T xa[8], xb[8], ya[8], yb[8];
         frag_k(As, Bs, 0, L, xa, xb);

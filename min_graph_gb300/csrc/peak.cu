@@ -136,7 +136,8 @@ __global__ void peak_kernel(const typename Op<V>::T* __restrict__ in, typename O
 //   11 fp32 fused, 12 fp32 min3, 13 fp32 packed.
 template <typename T, int CORE, int MINB>
 __global__ void __launch_bounds__(256, MINB)
-core_kernel(const T* __restrict__ in, T* __restrict__ out, long long* __restrict__ cycles, int iters) {
+core_kernel(const T* __restrict__ in, T* __restrict__ out, long long* __restrict__ cycles, int iters,
+            int one) {
     constexpr int KLEN = 32;
     extern __shared__ __align__(16) unsigned char core_smem[];
     T* As = reinterpret_cast<T*>(core_smem);
@@ -150,7 +151,7 @@ core_kernel(const T* __restrict__ in, T* __restrict__ out, long long* __restrict
 #pragma unroll
         for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = in[(ri * 8 + ci + threadIdx.x) & 255];
     const long long t0 = clock64();
-    for (int it = 0; it < iters; ++it) apsp::mm_core<T, CORE, KLEN>(acc, As, Bs, L);
+    for (int it = 0; it < iters; ++it) apsp::mm_core<T, CORE, KLEN>(acc, As, Bs, L, one);
     __syncthreads();
     const long long t1 = clock64();
     T r = acc[0][0];
@@ -185,9 +186,9 @@ int run_core(int blocks, int iters, double* rpc, double* ms_out, long long* tota
     if (e == cudaSuccess) e = cudaEventCreate(&e0);
     if (e == cudaSuccess) e = cudaEventCreate(&e1);
     if (e == cudaSuccess) {
-        core_kernel<T, CORE, MINB><<<blocks, threads, smem>>>(in, out, cyc, 1);
+        core_kernel<T, CORE, MINB><<<blocks, threads, smem>>>(in, out, cyc, 1, 1);
         cudaEventRecord(e0);
-        core_kernel<T, CORE, MINB><<<blocks, threads, smem>>>(in, out, cyc, iters);
+        core_kernel<T, CORE, MINB><<<blocks, threads, smem>>>(in, out, cyc, iters, 1);
         cudaEventRecord(e1);
         e = cudaEventSynchronize(e1);
     }
@@ -267,7 +268,7 @@ int run(int blocks, int threads, int iters, double* rpc, double* ms_out, long lo
 
 }  // namespace
 
-extern "C" int apsp_peak_variants(void) { return 16; }
+extern "C" int apsp_peak_variants(void) { return 21; }
 
 extern "C" int apsp_peak_addmin(int variant, int blocks, int threads, int iters, double* rpc,
                                 double* ms, long long* total) {
@@ -281,6 +282,11 @@ extern "C" int apsp_peak_addmin(int variant, int blocks, int threads, int iters,
         case 13: return run_core<float, apsp::kCorePacked>(blocks, iters, rpc, ms, total);
         case 14: return run_core<int32_t, apsp::kCoreFused, 2>(blocks, iters, rpc, ms, total);
         case 15: return run_core<float, apsp::kCorePacked, 2>(blocks, iters, rpc, ms, total);
+        case 16: return run_core<int32_t, apsp::kCoreMixAdd + 2>(blocks, iters, rpc, ms, total);
+        case 17: return run_core<int32_t, apsp::kCoreMixAdd + 3>(blocks, iters, rpc, ms, total);
+        case 18: return run_core<int32_t, apsp::kCoreMixMad + 2>(blocks, iters, rpc, ms, total);
+        case 19: return run_core<int32_t, apsp::kCoreMixMad + 3>(blocks, iters, rpc, ms, total);
+        case 20: return run_core<int32_t, apsp::kCoreMixMad + 4>(blocks, iters, rpc, ms, total);
         case 0: return run<0>(blocks, threads, iters, rpc, ms, total);
         case 1: return run<1>(blocks, threads, iters, rpc, ms, total);
         case 2: return run<2>(blocks, threads, iters, rpc, ms, total);

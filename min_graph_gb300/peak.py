@@ -25,6 +25,11 @@ VARIANTS = {
     13: "core: fp32 add.f32x2 + three-input min (smem-fed)",
     14: "core: int32 fused, compiled for 2 blocks/SM",
     15: "core: fp32 add.f32x2 + min3, compiled for 2 blocks/SM",
+    16: "core: int32 mixed, 2/8 rows fused add-min, rest adds + min3",
+    17: "core: int32 mixed, 3/8 rows fused add-min, rest adds + min3",
+    18: "core: int32 mixed, 2/8 rows fused, rest multiply-add adds + min3",
+    19: "core: int32 mixed, 3/8 rows fused, rest multiply-add adds + min3",
+    20: "core: int32 mixed, 4/8 rows fused, rest multiply-add adds + min3",
 }
 
 
