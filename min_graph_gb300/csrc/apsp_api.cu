@@ -166,6 +166,25 @@ bool persistent_phase3_allowed() {
     return !(v && std::strcmp(v, "cpasync") == 0);
 }
 
+// APSP_P3_COLS=4|8 picks the persistent phase 3's accumulator columns per
+// thread (512 or 256 consumer threads); the default is kDefaultP3Cols.
+constexpr int kDefaultP3Cols = 8;
+int phase3_cols() {
+    const char* v = std::getenv("APSP_P3_COLS");
+    if (v && std::strcmp(v, "4") == 0) return 4;
+    if (v && std::strcmp(v, "8") == 0) return 8;
+    return kDefaultP3Cols;
+}
+
+// APSP_P3_STAGES=4|5 picks the persistent phase 3's slab ring depth.
+constexpr int kDefaultP3Stages = 4;
+int phase3_stages() {
+    const char* v = std::getenv("APSP_P3_STAGES");
+    if (v && std::strcmp(v, "5") == 0) return 5;
+    if (v && std::strcmp(v, "4") == 0) return 4;
+    return kDefaultP3Stages;
+}
+
 bool args_ok(const void* p, int n, int ld) {
     if (n < 0 || n > APSP_MAX_N || ld < n) return false;
     if (n > 0 && p == nullptr) return false;
@@ -240,6 +259,8 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
     a.tma = 0;
     a.inject = 0;
     a.timeout_ns = kDefaultTimeoutNs;
+    a.p3_cols = phase3_cols();
+    a.p3_stages = phase3_stages();
     const bool is_float = std::is_same<T, float>::value;
     if (a.vec && nb > 1 && persistent_phase3_allowed()) {
         const int ks = apsp::phase3_slab_rows();

@@ -27,6 +27,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "mm_core.cuh"
@@ -38,7 +39,6 @@ constexpr int P1_THREADS = 512;    // phase 1: 128 rows x 4 quarters
 constexpr int MM_THREADS = 256;    // tile-product threads (8 warps)
 constexpr int KS = 32;             // k-slab depth in phase 3
 constexpr int P3_STAGES = 3;       // cp.async ring depth (fallback phase 3)
-constexpr int P1_QPAD = 36;        // phase 1 row buffer quarter stride (bank spread)
 
 template <typename T> struct Sem;
 
@@ -129,52 +129,66 @@ template <typename T> struct Core { static constexpr int value = kCoreFused; };
 //
 // Closure of the primary tile P = D[K,K] (Algorithm 16 of the thesis page:
 // standard Floyd-Warshall on the primary block, in shared memory, one
-// block).  Thread t owns row i = t/4 and the 32 columns of quarter q = t%4 in
-// registers.  At step k every thread needs P[i][k] and row k.  Their owners
-// publish them into a double-buffered shared row/column buffer after step
-// k-1, so each step needs one barrier.  Row k and column k do not change
-// during step k because P[k][k] >= 0.  The closed tile goes back to D and
-// into the workspace as prim (row-major) and primT (transposed), which
-// phase 2 reads.
+// block).  512 threads.  Each holds a 4 x 8 block of P in registers: rows
+// i0..i0+3 (i0 = 4 * (t / 16)) and columns j0..j0+7 (j0 = 8 * (t % 16)).
+// At step k a thread needs P[i][k] for its 4 rows (one 16-byte shared load)
+// and P[k][j] for its 8 columns (two), which is 32 relaxations per 3 loads.
+// The owners publish row k+1 and column k+1 into a double-buffered shared
+// row/column buffer right after step k, so each step needs one barrier.  Row
+// k and column k do not change during step k because P[k][k] >= 0.  The closed
+// tile goes back to D and into the workspace as prim (row-major) and primT
+// (transposed), which phase 2 reads.
 template <typename T>
 __global__ void __launch_bounds__(P1_THREADS, 1)
 fw_phase1_diag(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ prim,
                T* __restrict__ primT, int vec) {
-    __shared__ __align__(16) T rowbuf[2][4 * P1_QPAD];
+    __shared__ __align__(16) T rowbuf[2][TB];
     __shared__ __align__(16) T colbuf[2][TB];
-    const int t = threadIdx.x, i = t >> 2, q = t & 3;
+    const int t = threadIdx.x;
+    const int g = t >> 4;           // row group: rows 4g .. 4g+3
+    const int h = t & 15;           // column group: cols 8h .. 8h+7
+    const int i0 = 4 * g, j0 = 8 * h;
     const int k0 = r * TB;
-    T v[32];
+    T v[4][8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) gload4(D, ld, n, k0 + i, k0 + q * 32 + 4 * m, vec != 0, v + 4 * m);
-
-    if (i == 0) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) rowbuf[0][q * P1_QPAD + c] = v[c];
+    for (int ri = 0; ri < 4; ++ri) {
+        gload4(D, ld, n, k0 + i0 + ri, k0 + j0, vec != 0, &v[ri][0]);
+        gload4(D, ld, n, k0 + i0 + ri, k0 + j0 + 4, vec != 0, &v[ri][4]);
     }
-    if (q == 0) colbuf[0][i] = v[0];
+    // publish row 0 and column 0
+    if (g == 0) {
+        vstore4(&rowbuf[0][j0], v[0][0], v[0][1], v[0][2], v[0][3]);
+        vstore4(&rowbuf[0][j0 + 4], v[0][4], v[0][5], v[0][6], v[0][7]);
+    }
+    if (h == 0) vstore4(&colbuf[0][i0], v[0][0], v[1][0], v[2][0], v[3][0]);
     __syncthreads();
 
-    for (int kc = 0; kc < 4; ++kc) {
+#pragma unroll 1
+    for (int kc = 0; kc < TB / 8; ++kc) {
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk) {
-            const int k = kc * 32 + kk;
+        for (int kk = 0; kk < 8; ++kk) {
+            const int k = kc * 8 + kk;
             const int buf = kk & 1;  // == k & 1
-            const T a = colbuf[buf][i];
-            T b[32];
+            T a[4], b[8];
+            vload4(&colbuf[buf][i0], a);
+            vload4(&rowbuf[buf][j0], b);
+            vload4(&rowbuf[buf][j0 + 4], b + 4);
 #pragma unroll
-            for (int m = 0; m < 8; ++m) vload4(&rowbuf[buf][q * P1_QPAD + 4 * m], b + 4 * m);
+            for (int ri = 0; ri < 4; ++ri)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = Sem<T>::relax(v[c], a, b[c]);
+                for (int ci = 0; ci < 8; ++ci) v[ri][ci] = Sem<T>::relax(v[ri][ci], a[ri], b[ci]);
             if (k + 1 < TB) {
-                if (i == k + 1) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) rowbuf[buf ^ 1][q * P1_QPAD + c] = v[c];
+                // row k+1 lives in row group (k+1)/4 at register row (k+1)%4
+                const int rr = (kk + 1) & 3;  // == (k+1) % 4, a compile-time value
+                if (g == (k + 1) >> 2) {
+                    vstore4(&rowbuf[buf ^ 1][j0], v[rr][0], v[rr][1], v[rr][2], v[rr][3]);
+                    vstore4(&rowbuf[buf ^ 1][j0 + 4], v[rr][4], v[rr][5], v[rr][6], v[rr][7]);
                 }
-                if (kk < 31) {
-                    if (q == kc) colbuf[buf ^ 1][i] = v[(kk + 1) & 31];
+                // column k+1 lives in column group (k+1)/8 at register column (k+1)%8
+                if (kk < 7) {
+                    if (h == kc) vstore4(&colbuf[buf ^ 1][i0], v[0][kk + 1], v[1][kk + 1], v[2][kk + 1], v[3][kk + 1]);
                 } else {
-                    if (q == kc + 1) colbuf[buf ^ 1][i] = v[0];
+                    if (h == kc + 1) vstore4(&colbuf[buf ^ 1][i0], v[0][0], v[1][0], v[2][0], v[3][0]);
                 }
                 __syncthreads();
             }
@@ -182,14 +196,15 @@ fw_phase1_diag(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ pr
     }
 
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-        gstore4(D, ld, n, k0 + i, k0 + q * 32 + 4 * m, vec != 0, v[4 * m], v[4 * m + 1],
-                v[4 * m + 2], v[4 * m + 3]);
+    for (int ri = 0; ri < 4; ++ri) {
+        const int i = i0 + ri;
+        gstore4(D, ld, n, k0 + i, k0 + j0, vec != 0, v[ri][0], v[ri][1], v[ri][2], v[ri][3]);
+        gstore4(D, ld, n, k0 + i, k0 + j0 + 4, vec != 0, v[ri][4], v[ri][5], v[ri][6], v[ri][7]);
+        vstore4(prim + i * TB + j0, v[ri][0], v[ri][1], v[ri][2], v[ri][3]);
+        vstore4(prim + i * TB + j0 + 4, v[ri][4], v[ri][5], v[ri][6], v[ri][7]);
+    }
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-        vstore4(prim + i * TB + q * 32 + 4 * m, v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
-#pragma unroll
-    for (int c = 0; c < 32; ++c) primT[(q * 32 + c) * TB + i] = v[c];
+    for (int ci = 0; ci < 8; ++ci) vstore4(primT + (j0 + ci) * TB + i0, v[0][ci], v[1][ci], v[2][ci], v[3][ci]);
 }
 
 // ----------------------------------------------------------------- phase 2
@@ -199,61 +214,90 @@ fw_phase1_diag(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ pr
 // skips the primary tile the way the page's skipPrimaryBlock map does).
 //   row panel tile (K,J):    new = min(old, P (x) old)  -> As = P^T, Bs = old
 //   column panel tile (I,K): new = min(old, old (x) P)  -> As = old^T, Bs = P
-// The result goes to D and to the workspace panel that phase 3 reads: rowp
-// (TB x npad) as is, colpT (TB x npad) transposed.
+// The accumulators start from the old tile (read from D).  As holds all 128
+// k in shared memory.  The B operand streams in two 64-row halves, which
+// keeps the CTA at 96 KiB of shared memory, so two CTAs share an SM and one
+// CTA's loads overlap the other's compute.  The result goes to D and to the
+// workspace panel that phase 3 reads: rowp (TB x npad) as is, colpT
+// (TB x npad) transposed.
+constexpr int P2_KH = TB / 2;  // k rows per B half
+
 template <typename T>
-__global__ void __launch_bounds__(MM_THREADS, 1)
+__global__ void __launch_bounds__(MM_THREADS, (std::is_same<T, int32_t>::value ? 2 : 1))
 fw_phase2_panels(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ rowp,
                  T* __restrict__ colpT, const T* __restrict__ prim, const T* __restrict__ primT,
                  int npad, int vec) {
     extern __shared__ __align__(128) unsigned char p2_smem[];
-    T* As = reinterpret_cast<T*>(p2_smem);
-    T* Bs = As + TB * TB;
+    T* As = reinterpret_cast<T*>(p2_smem);  // [TB][TB]
+    T* Bs = As + TB * TB;                    // [P2_KH][TB]
     const int tid = threadIdx.x;
     const int bx = blockIdx.x;
     const int other = bx + (bx >= r ? 1 : 0);
     const int k0 = r * TB, t0 = other * TB;
     const bool is_row = (blockIdx.y == 0);
     const MMLayout L(tid);
-    T acc[8][8];
+    // Full, aligned tiles stage their straight copies with cp.async; ragged
+    // or unaligned tiles take element-wise loads.
+    const bool fast = vec != 0 && k0 + TB <= n && t0 + TB <= n;
+    const int orow0 = is_row ? k0 : t0, ocol0 = is_row ? t0 : k0;  // this CTA's tile in D
 
+    T acc[8][8];
+#pragma unroll
+    for (int ri = 0; ri < 8; ++ri) {
+        gload4(D, ld, n, orow0 + L.row(ri), ocol0 + L.cB0, vec != 0, &acc[ri][0]);
+        gload4(D, ld, n, orow0 + L.row(ri), ocol0 + L.cB1, vec != 0, &acc[ri][4]);
+    }
     if (is_row) {
-        for (int c = tid; c < TB * TB / 4; c += MM_THREADS) {
-            const int kk = c >> 5, qq = (c & 31) * 4;
-            T x[4];
-            vload4(primT + kk * TB + qq, x);
-            vstore4(As + kk * TB + qq, x[0], x[1], x[2], x[3]);
-            gload4(D, ld, n, k0 + kk, t0 + qq, vec != 0, x);
-            vstore4(Bs + kk * TB + qq, x[0], x[1], x[2], x[3]);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int ri = 0; ri < 8; ++ri)
-#pragma unroll
-            for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Bs[L.row(ri) * TB + L.col(ci)];
+        for (int c = tid; c < TB * TB / 4; c += MM_THREADS)
+            cp_async16(smem_u32(As + c * 4), primT + c * 4);
     } else {
-#pragma unroll
-        for (int ri = 0; ri < 8; ++ri) {
-            gload4(D, ld, n, t0 + L.row(ri), k0 + L.cB0, vec != 0, &acc[ri][0]);
-            gload4(D, ld, n, t0 + L.row(ri), k0 + L.cB1, vec != 0, &acc[ri][4]);
-        }
-        // transpose through registers: As[k][i] = old[i][k]
+        // transpose the old tile through registers: As[k][i] = old[i][k]
 #pragma unroll
         for (int ci = 0; ci < 8; ++ci) {
             const int k = L.col(ci);
             vstore4(As + k * TB + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
             vstore4(As + k * TB + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
         }
-        for (int c = tid; c < TB * TB / 4; c += MM_THREADS) {
-            const int kk = c >> 5, qq = (c & 31) * 4;
-            T x[4];
-            vload4(prim + kk * TB + qq, x);
-            vstore4(Bs + kk * TB + qq, x[0], x[1], x[2], x[3]);
-        }
-        __syncthreads();
     }
 
-    mm_core<T, Core<T>::value, TB>(acc, As, Bs, L);
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        const int kb = hh * P2_KH;
+        if (hh > 0) __syncthreads();  // everyone is done with the previous half
+        if (is_row) {
+            if (fast) {
+                for (int c = tid; c < P2_KH * TB / 4; c += MM_THREADS) {
+                    const int kk = c >> 5, qq = (c & 31) * 4;
+                    cp_async16(smem_u32(Bs + kk * TB + qq), D + (long long)(k0 + kb + kk) * ld + t0 + qq);
+                }
+            } else {
+                for (int c = tid; c < P2_KH * TB / 4; c += MM_THREADS) {
+                    const int kk = c >> 5, qq = (c & 31) * 4;
+                    T x[4];
+                    gload4(D, ld, n, k0 + kb + kk, t0 + qq, vec != 0, x);
+                    vstore4(Bs + kk * TB + qq, x[0], x[1], x[2], x[3]);
+                }
+            }
+        } else {
+            for (int c = tid; c < P2_KH * TB / 4; c += MM_THREADS)
+                cp_async16(smem_u32(Bs + c * 4), prim + kb * TB + c * 4);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        if constexpr (std::is_same<T, int32_t>::value) {
+            if (is_row && fast) {  // entries above INF read as INF
+                for (int c = tid; c < P2_KH * TB / 4; c += MM_THREADS) {
+                    T x[4];
+                    vload4(Bs + c * 4, x);
+                    vstore4(Bs + c * 4, Sem<T>::clamp(x[0]), Sem<T>::clamp(x[1]), Sem<T>::clamp(x[2]),
+                            Sem<T>::clamp(x[3]));
+                }
+                __syncthreads();
+            }
+        }
+        mm_core<T, Core<T>::value, P2_KH>(acc, As + kb * TB, Bs, L);
+    }
 
     if (is_row) {
 #pragma unroll
@@ -370,20 +414,28 @@ fw_phase3_minplus(T* __restrict__ D, long long ld, int n, int r, int nbm1,
 // from shared memory, run the paired-k product over the ring, and store the
 // result straight from registers.  Full/empty mbarriers order the two sides,
 // and every wait is bounded (tma.cuh).
-constexpr int P3P_CONSUMERS = MM_THREADS;
-constexpr int P3P_THREADS = P3P_CONSUMERS + 32;
-constexpr int P3P_STAGES = 4;
 constexpr uint32_t P3P_SLAB_BYTES = KS * TB * 4;             // 16 KiB per operand slab
 constexpr uint32_t P3P_STAGE_BYTES = 2 * P3P_SLAB_BYTES;     // A + B
 constexpr uint32_t P3P_C_BYTES = TB * TB * 4;                // 64 KiB
-constexpr size_t kPhase3PSmem = 1024 + P3P_C_BYTES + (size_t)P3P_STAGES * P3P_STAGE_BYTES + 256;
+// Shared memory of the persistent phase 3 with a ring of `stages` slabs.
+constexpr size_t phase3p_smem(int stages) {
+    return 1024 + P3P_C_BYTES + (size_t)stages * P3P_STAGE_BYTES + 256;
+}
 
-template <typename T>
-__global__ void __launch_bounds__(P3P_THREADS, 1)
+// NC = accumulator columns per consumer thread: 8 (256 consumers, 2 warps per
+// SM sub-partition) or 4 (512 consumers, 4 warps per sub-partition, which
+// hides barrier waits and epilogues better).
+template <int NC>
+constexpr int p3p_threads() { return TileMap<NC>::kThreads + 32; }
+
+template <typename T, int NC, int P3P_STAGES>
+__global__ void __launch_bounds__(p3p_threads<NC>(), 1)
 fw_phase3_persistent(T* __restrict__ D, long long ld, int n, int r, int nbm1, int ntiles,
                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_b, int* __restrict__ err,
                      unsigned long long timeout_ns, int inject) {
+    constexpr int CONSUMERS = TileMap<NC>::kThreads;
+    constexpr int CWARPS = CONSUMERS / 32;
     extern __shared__ unsigned char p3p_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(p3p_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -400,17 +452,17 @@ fw_phase3_persistent(T* __restrict__ D, long long ld, int n, int r, int nbm1, in
     if (tid == 0) {
         for (int s = 0; s < P3P_STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, P3P_CONSUMERS / 32);
+            mbar_init(bar_empty + 8 * s, CWARPS);
         }
         mbar_init(bar_cfull, 1);
-        mbar_init(bar_cempty, P3P_CONSUMERS / 32);
+        mbar_init(bar_cempty, CWARPS);
         mbar_init_fence();
     }
     __syncthreads();
 
-    if (tid >= P3P_CONSUMERS) {
+    if (tid >= CONSUMERS) {
         // ------------------------------------------------------ producer
-        if (tid != P3P_CONSUMERS) return;
+        if (tid != CONSUMERS) return;
         tma_prefetch_desc(&tm_c);
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
@@ -460,29 +512,27 @@ fw_phase3_persistent(T* __restrict__ D, long long ld, int n, int r, int nbm1, in
     }
 
     // ---------------------------------------------------------- consumers
-    const MMLayout L(tid);
+    const TileMap<NC> L(tid);
     const int lane = tid & 31;
     uint32_t g = 0;
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         int I, J;
         phase3_tile(t, nbm1, r, I, J);
-        T acc[8][8];
+        T acc[8][NC];
         if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
+        load_tile(acc, cbuf, L);
 #pragma unroll
-        for (int ri = 0; ri < 8; ++ri) {
-            vload4(cbuf + L.row(ri) * TB + L.cB0, &acc[ri][0]);
-            vload4(cbuf + L.row(ri) * TB + L.cB1, &acc[ri][4]);
+        for (int ri = 0; ri < 8; ++ri)
 #pragma unroll
-            for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
-        }
+            for (int ci = 0; ci < NC; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_cempty);
         for (int s = 0; s < NSLAB; ++s, ++g) {
             const uint32_t st = g % P3P_STAGES, use = g / P3P_STAGES;
             if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
             const T* As = reinterpret_cast<const T*>(ring + st * P3P_STAGE_BYTES);
-            mm_core<T, Core<T>::value, KS>(acc, As, As + KS * TB, L);
+            mm_core_fused<T, KS, NC>(acc, As, As + KS * TB, L);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * st);
         }
@@ -491,12 +541,13 @@ fw_phase3_persistent(T* __restrict__ D, long long ld, int n, int r, int nbm1, in
         for (int ri = 0; ri < 8; ++ri) {
             const int i = row0 + L.row(ri);
             gstore4(D, ld, n, i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-            gstore4(D, ld, n, i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            if constexpr (NC == 8)
+                gstore4(D, ld, n, i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
         }
     }
 }
 
-constexpr size_t kPhase2Smem = 2ull * TB * TB * 4;
+constexpr size_t kPhase2Smem = (size_t)(TB + P2_KH) * TB * 4;
 constexpr size_t kPhase3Smem = (size_t)P3_STAGES * 2 * KS * TB * 4;
 
 }  // namespace apsp

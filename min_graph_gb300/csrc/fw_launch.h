@@ -26,6 +26,8 @@ struct RoundArgs {
     int* err;       // device error word (bounded-wait timeouts)
     unsigned long long timeout_ns;  // bound on every device-side wait
     int inject;     // test hook: persistent phase 3 skips one slab (forces a timeout)
+    int p3_cols;    // persistent phase 3 accumulator columns per thread: 8 or 4
+    int p3_stages;  // persistent phase 3 slab ring depth: 4 or 5 (8 columns only)
     CUtensorMap tm_c;   // D, n x n, box TB x TB
     CUtensorMap tm_a;   // colpT, TB x npad, box KS x TB
     CUtensorMap tm_b;   // rowp,  TB x npad, box KS x TB

@@ -16,8 +16,14 @@ cudaError_t kernels_init_impl() {
     e = cudaFuncSetAttribute(fw_phase3_minplus<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPhase3Smem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(fw_phase3_persistent<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kPhase3PSmem);
+    e = cudaFuncSetAttribute(fw_phase3_persistent<T, 8, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)phase3p_smem(4));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fw_phase3_persistent<T, 8, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)phase3p_smem(5));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fw_phase3_persistent<T, 4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)phase3p_smem(4));
 }
 
 template <typename T>
@@ -43,9 +49,18 @@ cudaError_t launch_phase3_impl(const RoundArgs& a, int r, cudaStream_t s) {
     const unsigned tiles = (unsigned)(a.nb - 1) * (unsigned)(a.nb - 1);
     if (a.tma) {
         const unsigned grid = tiles < (unsigned)a.sms ? tiles : (unsigned)a.sms;
-        fw_phase3_persistent<T><<<grid, P3P_THREADS, kPhase3PSmem, s>>>(
-            static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, (int)tiles, a.tm_c, a.tm_a, a.tm_b, a.err,
-            a.timeout_ns, a.inject);
+        if (a.p3_cols == 4)
+            fw_phase3_persistent<T, 4, 4><<<grid, p3p_threads<4>(), phase3p_smem(4), s>>>(
+                static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, (int)tiles, a.tm_c, a.tm_a, a.tm_b,
+                a.err, a.timeout_ns, a.inject);
+        else if (a.p3_stages == 5)
+            fw_phase3_persistent<T, 8, 5><<<grid, p3p_threads<8>(), phase3p_smem(5), s>>>(
+                static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, (int)tiles, a.tm_c, a.tm_a, a.tm_b,
+                a.err, a.timeout_ns, a.inject);
+        else
+            fw_phase3_persistent<T, 8, 4><<<grid, p3p_threads<8>(), phase3p_smem(4), s>>>(
+                static_cast<T*>(a.d), a.ld, a.n, r, a.nb - 1, (int)tiles, a.tm_c, a.tm_a, a.tm_b,
+                a.err, a.timeout_ns, a.inject);
         return cudaGetLastError();
     }
     fw_phase3_minplus<T><<<tiles, MM_THREADS, kPhase3Smem, s>>>(

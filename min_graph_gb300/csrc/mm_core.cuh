@@ -48,26 +48,33 @@ constexpr int kCorePacked = 2;
 constexpr int kCoreMixAdd = 16;
 constexpr int kCoreMixMad = 32;
 
-// Thread layout of the 128 x 128 tile product: 8 warps as 4 (rows) x 2
-// (cols), each warp 32 x 64; inside a warp 4 x 8 lanes, each lane owning
-// rows {rA0..rA0+3, rA1..rA1+3} and cols {cB0..cB0+3, cB1..cB1+3}.  In the
-// k-major layout, for a fixed k the lanes of a warp read 4 distinct 16-byte A
-// chunks and 8 distinct B chunks, all within one shared-memory row: one
-// wavefront each.
-struct MMLayout {
+// Thread layouts of the 128 x 128 tile product.  Each thread owns 8 rows
+// {rA0..rA0+3, rA1..rA1+3} (rA1 = rA0 + 16) and NC columns:
+//   NC = 8: 256 threads, 8 warps as 4 (rows) x 2 (cols) of 32 x 64; columns
+//           {cB0..cB0+3, cB1..cB1+3} with cB1 = cB0 + 32.
+//   NC = 4: 512 threads, 16 warps as 4 x 4 of 32 x 32; columns cB0..cB0+3.
+// Inside a warp the lanes are 4 (rows) x 8 (cols).  In the k-major layout,
+// for a fixed k the lanes of a warp read 4 distinct 16-byte A chunks and 8
+// distinct B chunks, all within one shared-memory row: one wavefront each.
+template <int NC>
+struct TileMap {
+    static_assert(NC == 8 || NC == 4, "8 or 4 columns per thread");
+    static constexpr int kThreads = NC == 8 ? 256 : 512;
     int rA0, rA1, cB0, cB1;
-    __device__ __forceinline__ explicit MMLayout(int tid) {
+    __device__ __forceinline__ explicit TileMap(int tid) {
         const int w = tid >> 5, lane = tid & 31;
-        const int wr = w >> 1, wc = w & 1;
         const int tr = lane >> 3, tc = lane & 7;
+        const int wr = NC == 8 ? (w >> 1) : (w >> 2);
+        const int wc = NC == 8 ? (w & 1) : (w & 3);
         rA0 = wr * 32 + tr * 4;
         rA1 = rA0 + 16;
-        cB0 = wc * 64 + tc * 4;
+        cB0 = wc * (8 * NC) + tc * 4;
         cB1 = cB0 + 32;
     }
     __device__ __forceinline__ int row(int ri) const { return ri < 4 ? rA0 + ri : rA1 + (ri - 4); }
     __device__ __forceinline__ int col(int ci) const { return ci < 4 ? cB0 + ci : cB1 + (ci - 4); }
 };
+using MMLayout = TileMap<8>;
 
 // ------------------------------------------------------------ elementwise ops
 
@@ -143,13 +150,13 @@ __device__ __forceinline__ void lds2x64(const void* p, unsigned long long* o) {
 }
 
 // k-major layout: A at As[k * TB + i], B at Bs[k * TB + j].
-template <typename T>
+template <typename T, int NC>
 __device__ __forceinline__ void frag_k(const T* __restrict__ As, const T* __restrict__ Bs, int k,
-                                       const MMLayout& L, T* a, T* b) {
+                                       const TileMap<NC>& L, T* a, T* b) {
     lds4(As + k * TB + L.rA0, a);
     lds4(As + k * TB + L.rA1, a + 4);
     lds4(Bs + k * TB + L.cB0, b);
-    lds4(Bs + k * TB + L.cB1, b + 4);
+    if constexpr (NC == 8) lds4(Bs + k * TB + L.cB1, b + 4);
 }
 
 // k-pair interleaved layout: A at A2[(kp * TB + i) * 2 + (k & 1)], same for B.
@@ -171,12 +178,12 @@ __device__ __forceinline__ void frag_kp(const T* __restrict__ A2, const T* __res
 
 // ------------------------------------------------------------ cores
 
-template <typename T>
-__device__ __forceinline__ void step1(T (&acc)[8][8], const T* a, const T* b) {
+template <typename T, int NC>
+__device__ __forceinline__ void step1(T (&acc)[8][NC], const T* a, const T* b) {
 #pragma unroll
     for (int ri = 0; ri < 8; ++ri)
 #pragma unroll
-        for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = CoreOps<T>::relax1(acc[ri][ci], a[ri], b[ci]);
+        for (int ci = 0; ci < NC; ++ci) acc[ri][ci] = CoreOps<T>::relax1(acc[ri][ci], a[ri], b[ci]);
 }
 
 template <typename T>
@@ -219,6 +226,21 @@ __device__ __forceinline__ void step_mix(int32_t (&acc)[8][8], const int32_t* a0
 // acc = min(acc, A (x) B) over k in [0, KLEN).  As/Bs: k-major for the fused,
 // min3 and mixed cores, k-pair interleaved for the packed core.  `one` must
 // be 1 (used by the kCoreMixMad cores only).
+template <typename T, int KLEN, int NC>
+__device__ __forceinline__ void mm_core_fused(T (&acc)[8][NC], const T* __restrict__ As,
+                                              const T* __restrict__ Bs, const TileMap<NC>& L) {
+    static_assert(KLEN % 2 == 0, "even k-length");
+    T xa[8], xb[NC], ya[8], yb[NC];
+    frag_k(As, Bs, 0, L, xa, xb);
+#pragma unroll 1
+    for (int k = 0; k < KLEN; k += 2) {
+        frag_k(As, Bs, k + 1, L, ya, yb);
+        step1(acc, xa, xb);
+        if (k + 2 < KLEN) frag_k(As, Bs, k + 2, L, xa, xb);
+        step1(acc, ya, yb);
+    }
+}
+
 template <typename T, int CORE, int KLEN>
 __device__ __forceinline__ void mm_core(T (&acc)[8][8], const T* __restrict__ As,
                                         const T* __restrict__ Bs, const MMLayout& L, int one = 1) {
@@ -241,16 +263,7 @@ __device__ __forceinline__ void mm_core(T (&acc)[8][8], const T* __restrict__ As
             step_mix<R, MAD>(acc, ya0, yb0, ya1, yb1, one);
         }
     } else if constexpr (CORE == kCoreFused) {
-        static_assert(KLEN % 2 == 0, "even k-length");
-        T xa[8], xb[8], ya[8], yb[8];
-        frag_k(As, Bs, 0, L, xa, xb);
-#pragma unroll 1
-        for (int k = 0; k < KLEN; k += 2) {
-            frag_k(As, Bs, k + 1, L, ya, yb);
-            step1(acc, xa, xb);
-            if (k + 2 < KLEN) frag_k(As, Bs, k + 2, L, xa, xb);
-            step1(acc, ya, yb);
-        }
+        mm_core_fused<T, KLEN, 8>(acc, As, Bs, L);
     } else if constexpr (CORE == kCoreMin3) {
         static_assert(KLEN % 4 == 0, "k-length a multiple of 4");
         T xa0[8], xb0[8], xa1[8], xb1[8], ya0[8], yb0[8], ya1[8], yb1[8];
@@ -278,6 +291,18 @@ __device__ __forceinline__ void mm_core(T (&acc)[8][8], const T* __restrict__ As
             if (kp + 2 < KLEN / 2) frag_kp(As, Bs, kp + 2, L, xa, xb);
             step2p<T>(acc, ya, yb);
         }
+    }
+}
+
+// acc = the NC columns of this thread's 8 rows of a 128 x 128 row-major
+// tile in shared memory.
+template <typename T, int NC>
+__device__ __forceinline__ void load_tile(T (&acc)[8][NC], const T* __restrict__ tile,
+                                          const TileMap<NC>& L) {
+#pragma unroll
+    for (int ri = 0; ri < 8; ++ri) {
+        lds4(tile + L.row(ri) * TB + L.cB0, &acc[ri][0]);
+        if constexpr (NC == 8) lds4(tile + L.row(ri) * TB + L.cB1, &acc[ri][4]);
     }
 }
 

@@ -129,6 +129,8 @@ extern "C" apsp_status_t apsp_solve_noalloc(int32_t* dist, int n, int ld, apsp_s
     a.sms = slot->sms;
     a.inject = 0;
     a.timeout_ns = 2000000000ull;
+    a.p3_cols = 8;
+    a.p3_stages = 4;
     a.tma = 0;
     if (a.vec && nb > 1) {
         const int ks = apsp::phase3_slab_rows();

@@ -220,26 +220,25 @@ def test_empty_and_single():
     apsp.solve(t)
 
 
+PHASE3_VARIANTS = [("APSP_PHASE3", "cpasync"), ("APSP_P3_COLS", "8"), ("APSP_P3_COLS", "4")]
+
+
 @pytest.mark.parametrize("n", [129, 300, 1000, 2100])
-def test_both_phase3_kernels_agree(n, monkeypatch):
-    """The persistent TMA phase 3 (default for aligned matrices) and the
-    one-CTA-per-tile cp.async phase 3 give identical results."""
+def test_all_phase3_kernels_agree(n, monkeypatch):
+    """Every phase-3 kernel gives the oracle's result: the persistent TMA
+    kernel with 256 or 512 consumer threads, and the one-CTA-per-tile
+    cp.async kernel."""
     w = graphgen.er_i32(n, 0.02, 1, 1000, seed=n + 7)
     ref = oracle.fw_i32(w, threads=threads())
-    got_p, _ = gpu_solve(w)
-    monkeypatch.setenv("APSP_PHASE3", "cpasync")
-    got_c, _ = gpu_solve(w)
-    monkeypatch.delenv("APSP_PHASE3")
-    assert_i32_exact(got_p, ref, "persistent")
-    assert_i32_exact(got_c, ref, "cp.async")
     wf = graphgen.er_f32(n, 0.02, seed=n + 8)
     reff = oracle.fw_f64(wf, threads=threads())
-    gf_p, _ = gpu_solve(wf)
-    monkeypatch.setenv("APSP_PHASE3", "cpasync")
-    gf_c, _ = gpu_solve(wf)
-    monkeypatch.delenv("APSP_PHASE3")
-    assert_f32_close(gf_p, reff, "persistent f32")
-    assert_f32_close(gf_c, reff, "cp.async f32")
+    for var, val in PHASE3_VARIANTS:
+        monkeypatch.setenv(var, val)
+        got, _ = gpu_solve(w)
+        gotf, _ = gpu_solve(wf)
+        monkeypatch.delenv(var)
+        assert_i32_exact(got, ref, f"{var}={val}")
+        assert_f32_close(gotf, reff, f"{var}={val} f32")
 
 
 def test_bounded_wait_timeout_is_reported_and_context_survives():
