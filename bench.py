@@ -200,7 +200,7 @@ def reference_arm(args, rank):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("fw_kernels.cuh", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"):
+    for f in ("fw_kernels.cuh", "fw_fused.cuh", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"):
         with open(os.path.join(ROOT, "min_graph_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -219,6 +219,21 @@ def phase3_traffic(n: int):
         return None
     nb = -(-n // TB)
     return rec["dram_bytes_per_tile"] * (nb - 1) ** 2 / 1e9  # GB per launch
+
+
+def fused_traffic(n: int):
+    """DRAM bytes per fw_round_fused launch from the committed ncu summary,
+    scaled by work items; None when the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "fw_round_fused_er8192_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    if rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    nb = -(-n // TB)
+    return rec["dram_bytes_per_item"] * nb * nb / 1e9  # GB per (full lookahead) launch
 
 
 def ours(args, rank, world, local):
@@ -258,7 +273,8 @@ def ours(args, rank, world, local):
     apsp.stream_check(stream)
 
     nb = -(-n // TB)
-    launches_per_solve = nb + (2 * nb if nb > 1 else 0)
+    fused_schedule = os.environ.get("APSP_FUSED", "1") != "0"
+    launches_per_solve = (nb + 1) if fused_schedule else nb + (2 * nb if nb > 1 else 0)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     apsp.phase_timing_read()
@@ -331,18 +347,26 @@ def ours(args, rank, world, local):
     clk = clocks.summary()
     f_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
     f_load = (clk or {}).get("sm_mhz")
+    fused = phase_cnt[0] == 0 and phase_cnt[2] > 0
     p3_launches = phase_cnt[2]
     p3_ms = phase_ms[2] / p3_launches if p3_launches else None
-    p3_relax = float(nb - 1) ** 2 * TB ** 3 if nb > 1 else 0.0
+    npad = nb * TB
+    if fused:
+        # round-fused schedule: all of a solve's npad^3 relaxations (phases 1-3)
+        # run in its nb + 1 launches of fw_round_fused
+        kernel = "fw_round_fused"
+        p3_relax = float(npad) ** 3 / (nb + 1)
+    else:
+        kernel = ("fw_phase3_minplus" if os.environ.get("APSP_PHASE3") == "cpasync"
+                  else "fw_phase3_persistent")
+        p3_relax = float(nb - 1) ** 2 * TB ** 3 if nb > 1 else 0.0
     ops_per_relax = 1 if dtype == torch.int32 else 2
     peak_tops = sms * NOMINAL_INT32_LANES * f_max * 1e6 / ops_per_relax / 1e12
     roof = None
     if p3_ms:
         achieved = p3_relax / (p3_ms * 1e-3) / 1e12
-        traffic = phase3_traffic(n)
+        traffic = phase3_traffic(n) if not fused else fused_traffic(n)
         measured_tops = sms * MEASURED_ADDMIN_PER_CLK * f_max * 1e6 / 1e12
-        kernel = ("fw_phase3_minplus" if os.environ.get("APSP_PHASE3") == "cpasync"
-                  else "fw_phase3_persistent")
         roof = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Trelax/s",
                 "frac": achieved / peak_tops, "traffic": traffic,
                 "traffic_unit": "GB per launch (DRAM read + write, scaled from the committed ncu capture)",

@@ -13,8 +13,10 @@ extern "C" {
 
 /*
  * apsp_debug_inject_phase3_timeout -- arm a one-shot fault for the next
- * solve that runs the persistent (TMA) phase 3.  In its first phase-3 launch,
- * CTA 0's producer skips issuing its first k-slab.  The consumers' bounded
+ * solve that runs a persistent TMA kernel: the persistent phase 3 of the
+ * three-kernel schedule, or the round-fused kernel.  In the first such launch
+ * with k-slabs (the first phase-3 launch, or round 0's fused launch), CTA 0's
+ * producer skips issuing its first k-slab.  The consumers' bounded
  * wait for that slab then runs out after `timeout_ns`: they record a timeout
  * in the device error word and leave, and the producer waits (also bounded)
  * for its copies still in flight before it leaves.  No fault, trap or

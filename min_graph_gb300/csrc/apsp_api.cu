@@ -185,6 +185,13 @@ int phase3_stages() {
     return kDefaultP3Stages;
 }
 
+// APSP_FUSED=0 selects the three-kernel schedule (phase 1, phase 2 and phase 3
+// as separate launches per round) instead of the round-fused one.
+bool fused_allowed() {
+    const char* v = std::getenv("APSP_FUSED");
+    return !(v && std::strcmp(v, "0") == 0);
+}
+
 bool args_ok(const void* p, int n, int ld) {
     if (n < 0 || n > APSP_MAX_N || ld < n) return false;
     if (n > 0 && p == nullptr) return false;
@@ -272,31 +279,102 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
     }
 
     const bool timed = g_timing.enabled && !capturing;
+    auto timed_launch = [&](int slot, auto&& launch) -> cudaError_t {
+        cudaEvent_t e0 = nullptr, e1 = nullptr;
+        if (timed) {
+            e0 = timing_event();
+            e1 = timing_event();
+            if (e0) cudaEventRecord(e0, s);
+        }
+        cudaError_t le = launch();
+        if (timed && e0 && e1) {
+            cudaEventRecord(e1, s);
+            g_timing.pending[slot].emplace_back(e0, e1);
+        }
+        return le;
+    };
+
+    if (a.tma && fused_allowed()) {
+        // Round-fused schedule: a prologue launch (phase 1 and 2 of round 0),
+        // then one launch per round (phase 3 of r with phase 1 and 2 of r+1).
+        apsp::FusedArgs f;
+        f.d = d;
+        f.ld = ld;
+        f.n = n;
+        f.nb = nb;
+        f.npad = npad;
+        f.sms = st.sms;
+        f.timeout_ns = kDefaultTimeoutNs;
+        f.inject = 0;
+        char* x = w + kErrBytes + (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * sizeof(T);
+        f.ptrs.rowp[0] = a.rowp;
+        f.ptrs.colpT[0] = a.colpT;
+        f.ptrs.rowp[1] = x;
+        f.ptrs.colpT[1] = x + (size_t)kTB * npad * sizeof(T);
+        f.ptrs.prim = a.prim;
+        f.ptrs.primT = a.primT;
+        int* flags = reinterpret_cast<int*>(x + 2 * (size_t)kTB * npad * sizeof(T));
+        f.ptrs.flag_diag = flags;
+        f.ptrs.flag_p1 = flags + 1;
+        f.ptrs.flag_row = flags + 2;
+        f.ptrs.flag_col = flags + 2 + nb;
+        f.ptrs.counters = flags + 2 + 2 * nb;
+        f.ptrs.err = a.err;
+        const int ks = apsp::phase3_slab_rows();
+        const unsigned long long pitch = (unsigned long long)npad * sizeof(T);
+        bool ok = true;
+        f.maps.c = a.tm_c;
+        for (int b = 0; b < 2; ++b) {
+            ok = ok && encode_2d(&f.maps.rowp[b], is_float, f.ptrs.rowp[b], npad, kTB, pitch, kTB, ks);
+            ok = ok && encode_2d(&f.maps.colpT[b], is_float, f.ptrs.colpT[b], npad, kTB, pitch, kTB, ks);
+        }
+        ok = ok && encode_2d(&f.maps.prim, is_float, a.prim, kTB, kTB, kTB * sizeof(T), kTB, ks);
+        ok = ok && encode_2d(&f.maps.primT, is_float, a.primT, kTB, kTB, kTB * sizeof(T), kTB, ks);
+        if (ok) {
+            // flags start at -1 (no round stamped yet), counters at 0
+            e = cudaMemsetAsync(flags, 0xFF, (size_t)(2 + 2 * nb) * sizeof(int), s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(f.ptrs.counters, 0, (size_t)(nb + 1) * sizeof(int), s);
+            if (e != cudaSuccess) return cuda_fail(e);
+            for (int r = -1; r < nb; ++r) {
+                const bool inject_here = (r == 0 && g_inject);
+                if (inject_here) {
+                    f.inject = 1;
+                    f.timeout_ns = g_inject_timeout_ns;
+                    g_inject = 0;
+                }
+                e = timed_launch(2, [&] { return apsp::launch_fused<T>(f, r, s); });
+                if (inject_here) {
+                    f.inject = 0;
+                    f.timeout_ns = kDefaultTimeoutNs;
+                }
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            if (!capturing) {
+                e = cudaEventRecord(st.done, s);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            return APSP_OK;
+        }
+    }
+
     for (int r = 0; r < nb; ++r) {
         for (int phase = 0; phase < 3; ++phase) {
             if (phase > 0 && nb < 2) break;
-            cudaEvent_t e0 = nullptr, e1 = nullptr;
-            if (timed) {
-                e0 = timing_event();
-                e1 = timing_event();
-                if (e0) cudaEventRecord(e0, s);
-            }
-            const bool inject_here = (phase == 2 && g_inject && a.tma);
-            if (inject_here) {
-                a.inject = 1;
-                a.timeout_ns = g_inject_timeout_ns;
-                g_inject = 0;
-            }
-            e = launch_phase<T>(phase, a, r, s);
-            if (inject_here) {
-                a.inject = 0;
-                a.timeout_ns = kDefaultTimeoutNs;
-            }
+            e = timed_launch(phase, [&] {
+                const bool inject_here = (phase == 2 && g_inject && a.tma);
+                if (inject_here) {
+                    a.inject = 1;
+                    a.timeout_ns = g_inject_timeout_ns;
+                    g_inject = 0;
+                }
+                cudaError_t le = launch_phase<T>(phase, a, r, s);
+                if (inject_here) {
+                    a.inject = 0;
+                    a.timeout_ns = kDefaultTimeoutNs;
+                }
+                return le;
+            });
             if (e != cudaSuccess) return cuda_fail(e);
-            if (timed && e0 && e1) {
-                cudaEventRecord(e1, s);
-                g_timing.pending[phase].emplace_back(e0, e1);
-            }
         }
     }
     if (!capturing) {
@@ -404,7 +482,10 @@ namespace apsp {
 size_t workspace_bytes(int n) {
     const size_t nb = (size_t)(n + kTB - 1) / kTB;
     const size_t npad = nb * kTB;
-    return kErrBytes + (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
+    const size_t base = kErrBytes + (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
+    const size_t panels2 = 2 * (size_t)kTB * npad * 4;       // second row/column panel buffers
+    const size_t flags = ((3 * nb + 3) * 4 + 255) / 256 * 256;  // flags + counters
+    return base + panels2 + flags;
 }
 }  // namespace apsp
 

@@ -1,0 +1,488 @@
+// Round-fused persistent blocked Floyd-Warshall (lookahead), sm_103a.
+//
+// The three phases of the thesis page (1library.co excerpt, section 4.6,
+// Algorithms 16-18) keep their arithmetic; what changes is the scheduling.
+// Launch r runs, on one CTA per SM, the phase-3 tiles of round r together
+// with phase 1 and phase 2 of round r+1:
+//
+//   l in [0, c1)        phase 3 (round r): the tiles in row r+1 and column
+//                       r+1 ("critical"; the diagonal (r+1, r+1) first)
+//   l = c1              phase 1 (round r+1): close tile (r+1, r+1)
+//   next x items        phase 3 (round r): ordinary tiles
+//   next 2(nb-1) items  phase 2 (round r+1): row panel (r+1, J), column
+//                       panel (I, r+1)
+//   the rest            phase 3 (round r): ordinary tiles
+//
+// CTAs take items in this order from a global counter.  Each item depends
+// only on items before it: phase 1 of r+1 on the critical tile (r+1, r+1),
+// and a phase-2 item on phase 1 of r+1 and on its own critical tile.  So
+// whichever CTAs are running always make progress, and no deadlock is
+// possible.  Waits on those dependencies are bounded spins on round-stamped
+// flags in global memory.  Phase 1 and phase 2 of round r+1 thus run inside
+// round r's phase-3 work, instead of as two latency-bound launches between
+// rounds.  The row/column panel buffers alternate between rounds, so phase 2
+// of r+1 never overwrites what phase 3 of r is reading.  A prologue launch
+// (r = -1) runs phase 1 and phase 2 of round 0; the last launch runs phase 3
+// only.
+//
+// Each CTA is one producer warp (an elected thread takes items, waits for
+// their inputs, and issues TMA loads) and eight consumer warps (the
+// arithmetic, on the tile-product core of mm_core.cuh).
+//   phase-3 tile:  C <- D tile; A slabs <- column panel; B slabs <- row panel
+//   row panel:     C <- D tile (also the B operand, read in shared memory);
+//                  A slabs <- transposed closed primary tile
+//   column panel:  C <- D tile; the consumers write its transpose into the
+//                  ring as the A operand; B slabs <- closed primary tile
+//   phase 1:       C <- D tile; closed in registers with a published row and
+//                  column per step (as fw_phase1_diag)
+// A TMA load of a tile that crosses the edge of the matrix reads zeros
+// outside it.  Phase-1 and phase-2 items overwrite those positions with INF
+// before using them; phase 3 never stores them.
+#pragma once
+
+#include "fw_kernels.cuh"
+#include "fw_launch.h"
+
+namespace apsp {
+
+constexpr int FZ_STAGES = 4;
+constexpr int FZ_CONSUMERS = 256;
+constexpr int FZ_THREADS = FZ_CONSUMERS + 32;
+constexpr uint32_t FZ_SLAB = KS * TB * 4;       // 16 KiB
+constexpr uint32_t FZ_STAGE = 2 * FZ_SLAB;      // A half + B half
+constexpr uint32_t FZ_C = TB * TB * 4;          // 64 KiB
+constexpr uint32_t FZ_MISC = 4096;              // barriers, item slots, phase-1 buffers
+constexpr size_t kFusedSmem = 1024 + FZ_C + (size_t)FZ_STAGES * FZ_STAGE + FZ_MISC;
+constexpr int FZ_NAMED_BAR = 1;                 // consumer-only named barrier id
+
+enum : int { kItemP3 = 0, kItemP1 = 1, kItemP2Row = 2, kItemP2Col = 3 };
+enum : int { kCritNone = 0, kCritDiag = 1, kCritRow = 2, kCritCol = 3 };
+
+struct FusedItem {
+    int kind, I, J, crit;
+};
+
+// Number of items of launch r (r = -1: prologue).
+__host__ __device__ inline long long fused_items(int r, int nb) {
+    if (r < 0) return 1 + 2LL * (nb - 1);
+    if (r + 1 >= nb) return (long long)(nb - 1) * (nb - 1);
+    return (long long)nb * nb;
+}
+
+// Ordinary phase-3 tiles taken before phase 2 of round r+1: enough work for
+// the other CTAs while one CTA runs phase 1 of r+1.
+__host__ __device__ inline int fused_head(int nb, int grid) {
+    const long long reg = (long long)(nb - 2) * (nb - 2);
+    const long long want = 3LL * grid;
+    return (int)(reg < want ? reg : want);
+}
+
+__device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x) {
+    FusedItem it;
+    it.crit = kCritNone;
+    const int rn = r + 1;
+    if (r < 0) {  // prologue: phase 1 and phase 2 of round 0
+        if (l == 0) { it.kind = kItemP1; it.I = it.J = 0; return it; }
+        const int q = l - 1;
+        if (q < nb - 1) { it.kind = kItemP2Row; it.I = 0; it.J = q + 1; }
+        else { it.kind = kItemP2Col; it.I = q - (nb - 1) + 1; it.J = 0; }
+        return it;
+    }
+    if (rn >= nb) {  // last round: phase 3 only
+        it.kind = kItemP3;
+        phase3_tile(l, nb - 1, r, it.I, it.J);
+        return it;
+    }
+    const int c1 = 2 * nb - 3;
+    if (l < c1) {
+        it.kind = kItemP3;
+        if (l == 0) { it.I = it.J = rn; it.crit = kCritDiag; }
+        else if (l < nb - 1) { const int q = l - 1; it.I = rn; it.J = q + (q >= r ? 2 : 0); it.crit = kCritRow; }
+        else { const int q = l - (nb - 1); it.I = q + (q >= r ? 2 : 0); it.J = rn; it.crit = kCritCol; }
+        return it;
+    }
+    l -= c1;
+    if (l == 0) { it.kind = kItemP1; it.I = it.J = rn; return it; }
+    l -= 1;
+    const int np2 = 2 * (nb - 1);
+    int q;
+    if (l < x) {
+        q = l;
+    } else if (l < x + np2) {
+        const int p = l - x;
+        if (p < nb - 1) { it.kind = kItemP2Row; it.I = rn; it.J = p + (p >= rn ? 1 : 0); }
+        else { const int pp = p - (nb - 1); it.kind = kItemP2Col; it.I = pp + (pp >= rn ? 1 : 0); it.J = rn; }
+        return it;
+    } else {
+        q = l - np2;
+    }
+    it.kind = kItemP3;
+    const int nb2 = nb > 2 ? nb - 2 : 1;  // ordinary tiles exist only when nb > 2
+    const int ti = q / nb2, tj = q - ti * nb2;
+    it.I = ti + (ti >= r ? 2 : 0);
+    it.J = tj + (tj >= r ? 2 : 0);
+    return it;
+}
+
+__device__ __forceinline__ void consumer_barrier() {
+    asm volatile("bar.sync %0, %1;" ::"n"(FZ_NAMED_BAR), "n"(FZ_CONSUMERS) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *flag == value (bounded).  Afterwards the data published with
+// the flag is visible to this thread and to its later TMA (async proxy) reads.
+__device__ __forceinline__ bool flag_wait(const int* flag, int value, int* err,
+                                          unsigned long long timeout_ns) {
+    if (ld_acquire(flag) != value) {
+        const unsigned long long t0 = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            __nanosleep(64);
+            if (ld_acquire(flag) == value) break;
+            if ((it & 31u) == 0u) {
+                if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+                if (global_timer_ns() - t0 > timeout_ns) {
+                    atomicOr(err, kDeviceErrTimeout);
+                    return false;
+                }
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// All consumer threads have issued their global stores for this item:
+// publish them (GPU scope, and to the async proxy) and set *flag = value.
+__device__ __forceinline__ void flag_signal(int* flag, int value) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    consumer_barrier();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicExch(flag, value);
+    }
+}
+
+// Set the positions of this thread's 8 x 8 block that fall outside the n x n
+// matrix to INF (tile at D[row0.., col0..]).
+template <typename T>
+__device__ __forceinline__ void mask_outside(T (&acc)[8][8], const MMLayout& L, int row0, int col0,
+                                             int n) {
+    if (row0 + TB <= n && col0 + TB <= n) return;
+#pragma unroll
+    for (int ri = 0; ri < 8; ++ri)
+#pragma unroll
+        for (int ci = 0; ci < 8; ++ci)
+            if (row0 + L.row(ri) >= n || col0 + L.col(ci) >= n) acc[ri][ci] = Sem<T>::inf();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(FZ_THREADS, 1)
+fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, int nitems,
+               const __grid_constant__ FusedMaps maps, const FusedPtrs ptrs,
+               unsigned long long timeout_ns, int inject) {
+    extern __shared__ unsigned char fz_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(fz_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    T* cbuf = reinterpret_cast<T*>(base);
+    unsigned char* ring = base + FZ_C;
+    unsigned char* misc = ring + FZ_STAGES * FZ_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+    volatile int* slots = reinterpret_cast<volatile int*>(misc + 128);
+    T* p1row = reinterpret_cast<T*>(misc + 1024);  // [2][TB]
+    T* p1col = p1row + 2 * TB;                      // [2][TB]
+    const uint32_t bar_full = smem_u32(bars);
+    const uint32_t bar_empty = bar_full + 8 * FZ_STAGES;
+    const uint32_t bar_cfull = bar_empty + 8 * FZ_STAGES;
+    const uint32_t bar_cempty = bar_cfull + 8;
+    const int tid = threadIdx.x;
+    const int rn = r + 1;
+    const int x = fused_head(nb, gridDim.x);
+    int* err = ptrs.err;
+
+    if (tid == 0) {
+        for (int s = 0; s < FZ_STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, FZ_CONSUMERS / 32);
+        }
+        mbar_init(bar_cfull, 1);
+        mbar_init(bar_cempty, FZ_CONSUMERS / 32);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (tid >= FZ_CONSUMERS) {
+        // ================================================== producer
+        if (tid != FZ_CONSUMERS) return;
+        const uint32_t cdst = smem_u32(cbuf);
+        const uint32_t rdst = smem_u32(ring);
+        const int pb = r & 1, nbuf = rn & 1;  // panel buffers read / written
+        uint32_t g = 0;
+        int it = 0;
+        bool ok = true;
+        for (;;) {
+            const int l = atomicAdd(ptrs.counters + rn, 1);
+            const bool stop = l >= nitems;
+            FusedItem w;
+            w.kind = kItemP3;
+            w.I = w.J = 0;
+            w.crit = kCritNone;
+            if (!stop) {
+                w = fused_item(l, r, nb, x);
+                if (w.kind == kItemP1 && r >= 0)
+                    ok = flag_wait(ptrs.flag_diag, rn, err, timeout_ns);
+                else if (w.kind == kItemP2Row)
+                    ok = flag_wait(ptrs.flag_p1, rn, err, timeout_ns) &&
+                         (r < 0 || w.J == r || flag_wait(ptrs.flag_row + w.J, rn, err, timeout_ns));
+                else if (w.kind == kItemP2Col)
+                    ok = flag_wait(ptrs.flag_p1, rn, err, timeout_ns) &&
+                         (r < 0 || w.I == r || flag_wait(ptrs.flag_col + w.I, rn, err, timeout_ns));
+            }
+            if (it > 0 && !mbar_wait_bounded(bar_cempty, (it - 1) & 1, err, timeout_ns)) ok = false;
+            if (stop || !ok) {
+                slots[it & 1] = -1;
+                mbar_arrive(bar_cfull);  // no bytes expected: releases the consumers
+                break;
+            }
+            slots[it & 1] = l;
+            mbar_arrive_expect_tx(bar_cfull, FZ_C);
+            tma_load_2d(cdst, &maps.c, w.J * TB, w.I * TB, bar_cfull);
+            ++it;
+            if (w.kind == kItemP1) continue;  // no slabs
+            for (int s = 0; s < TB / KS; ++s) {
+                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
+                if (use > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1, err, timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (inject && g == 0 && blockIdx.x == 0) {
+                    // Test hook: this slab is never issued, so the consumers'
+                    // bounded wait on it must run out (APSP_ETIMEOUT).
+                    ++g;
+                    continue;
+                }
+                const uint32_t dst = rdst + st * FZ_STAGE;
+                if (w.kind == kItemP3) {
+                    mbar_arrive_expect_tx(bar_full + 8 * st, FZ_STAGE);
+                    tma_load_2d(dst, &maps.colpT[pb], w.I * TB, s * KS, bar_full + 8 * st);
+                    tma_load_2d(dst + FZ_SLAB, &maps.rowp[pb], w.J * TB, s * KS, bar_full + 8 * st);
+                } else if (w.kind == kItemP2Row) {
+                    mbar_arrive_expect_tx(bar_full + 8 * st, FZ_SLAB);
+                    tma_load_2d(dst, &maps.primT, 0, s * KS, bar_full + 8 * st);
+                } else {
+                    mbar_arrive_expect_tx(bar_full + 8 * st, FZ_SLAB);
+                    tma_load_2d(dst + FZ_SLAB, &maps.prim, 0, s * KS, bar_full + 8 * st);
+                }
+                ++g;
+            }
+            if (!ok) break;
+        }
+        (void)nbuf;
+        if (!ok) {
+            // Drain every copy still in flight before the CTA may exit.
+            for (uint32_t q = (g > FZ_STAGES ? g - FZ_STAGES : 0); q < g; ++q)
+                mbar_wait_bounded(bar_full + 8 * (q % FZ_STAGES), (q / FZ_STAGES) & 1, err, timeout_ns,
+                                  false);
+            if (it > 0) mbar_wait_bounded(bar_cfull, (it - 1) & 1, err, timeout_ns, false);
+        }
+        return;
+    }
+
+    // ====================================================== consumers
+    const MMLayout L(tid);
+    const int lane = tid & 31;
+    const int pb = r & 1, nbuf = rn & 1;
+    uint32_t g = 0;
+    for (int it = 0;; ++it) {
+        if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
+        const int l = slots[it & 1];
+        if (l < 0) return;
+        const FusedItem w = fused_item(l, r, nb, x);
+        const int row0 = w.I * TB, col0 = w.J * TB;
+
+        if (w.kind == kItemP1) {
+            // ------------------------------------------------ phase 1 (round rn)
+            // 16 x 16 thread grid, 8 x 8 per thread: rows 8 gq.., cols 8 hq..
+            const int gq = tid >> 4, hq = tid & 15;
+            const int i0 = 8 * gq, j0 = 8 * hq;
+            T v[8][8];
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                lds4(cbuf + (i0 + ri) * TB + j0, &v[ri][0]);
+                lds4(cbuf + (i0 + ri) * TB + j0 + 4, &v[ri][4]);
+#pragma unroll
+                for (int ci = 0; ci < 8; ++ci) {
+                    v[ri][ci] = Sem<T>::clamp(v[ri][ci]);
+                    if (row0 + i0 + ri >= n || col0 + j0 + ci >= n) v[ri][ci] = Sem<T>::inf();
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);
+            if (gq == 0) {
+                vstore4(p1row + j0, v[0][0], v[0][1], v[0][2], v[0][3]);
+                vstore4(p1row + j0 + 4, v[0][4], v[0][5], v[0][6], v[0][7]);
+            }
+            if (hq == 0) {
+                vstore4(p1col + i0, v[0][0], v[1][0], v[2][0], v[3][0]);
+                vstore4(p1col + i0 + 4, v[4][0], v[5][0], v[6][0], v[7][0]);
+            }
+            consumer_barrier();
+#pragma unroll 1
+            for (int kc = 0; kc < TB / 8; ++kc) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int k = kc * 8 + kk;
+                    const int buf = kk & 1;
+                    T a[8], b[8];
+                    lds4(p1col + buf * TB + i0, a);
+                    lds4(p1col + buf * TB + i0 + 4, a + 4);
+                    lds4(p1row + buf * TB + j0, b);
+                    lds4(p1row + buf * TB + j0 + 4, b + 4);
+#pragma unroll
+                    for (int ri = 0; ri < 8; ++ri)
+#pragma unroll
+                        for (int ci = 0; ci < 8; ++ci) v[ri][ci] = Sem<T>::relax(v[ri][ci], a[ri], b[ci]);
+                    if (k + 1 < TB) {
+                        const int rr = (kk + 1) & 7;  // compile-time register row/column of k+1
+                        const int grp = kk < 7 ? kc : kc + 1;
+                        if (gq == grp) {
+                            vstore4(p1row + (buf ^ 1) * TB + j0, v[rr][0], v[rr][1], v[rr][2], v[rr][3]);
+                            vstore4(p1row + (buf ^ 1) * TB + j0 + 4, v[rr][4], v[rr][5], v[rr][6], v[rr][7]);
+                        }
+                        if (hq == grp) {
+                            vstore4(p1col + (buf ^ 1) * TB + i0, v[0][rr], v[1][rr], v[2][rr], v[3][rr]);
+                            vstore4(p1col + (buf ^ 1) * TB + i0 + 4, v[4][rr], v[5][rr], v[6][rr], v[7][rr]);
+                        }
+                        consumer_barrier();
+                    }
+                }
+            }
+            T* prim = static_cast<T*>(ptrs.prim);
+            T* primT = static_cast<T*>(ptrs.primT);
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                const int i = i0 + ri;
+                gstore4(D, ld, n, row0 + i, col0 + j0, true, v[ri][0], v[ri][1], v[ri][2], v[ri][3]);
+                gstore4(D, ld, n, row0 + i, col0 + j0 + 4, true, v[ri][4], v[ri][5], v[ri][6], v[ri][7]);
+                vstore4(prim + i * TB + j0, v[ri][0], v[ri][1], v[ri][2], v[ri][3]);
+                vstore4(prim + i * TB + j0 + 4, v[ri][4], v[ri][5], v[ri][6], v[ri][7]);
+            }
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+                vstore4(primT + (j0 + ci) * TB + i0, v[0][ci], v[1][ci], v[2][ci], v[3][ci]);
+                vstore4(primT + (j0 + ci) * TB + i0 + 4, v[4][ci], v[5][ci], v[6][ci], v[7][ci]);
+            }
+            flag_signal(ptrs.flag_p1, rn);
+            continue;
+        }
+
+        T acc[8][8];
+        load_tile(acc, cbuf, L);
+#pragma unroll
+        for (int ri = 0; ri < 8; ++ri)
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
+
+        if (w.kind == kItemP3) {
+            // ------------------------------------------------ phase 3 (round r)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);
+            for (int s = 0; s < TB / KS; ++s, ++g) {
+                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
+                if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
+                const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
+                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                const int i = row0 + L.row(ri);
+                gstore4(D, ld, n, i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                gstore4(D, ld, n, i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            }
+            if (w.crit == kCritDiag) flag_signal(ptrs.flag_diag, rn);
+            else if (w.crit == kCritRow) flag_signal(ptrs.flag_row + w.J, rn);
+            else if (w.crit == kCritCol) flag_signal(ptrs.flag_col + w.I, rn);
+        } else if (w.kind == kItemP2Row) {
+            // -------------------------------- phase 2, row panel tile (rn, J)
+            // B is the tile itself: put the clamped, edge-masked values back in
+            // the shared buffer, then run the product over A slabs (P^T).
+            mask_outside(acc, L, row0, col0, n);
+            consumer_barrier();  // every warp has read the raw tile
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                vstore4(cbuf + L.row(ri) * TB + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                vstore4(cbuf + L.row(ri) * TB + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            }
+            // the buffer is refilled by TMA later: order these writes first
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            consumer_barrier();
+            for (int s = 0; s < TB / KS; ++s, ++g) {
+                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
+                if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
+                const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
+                mm_core_fused<T, KS, 8>(acc, As, cbuf + s * KS * TB, L);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);
+            T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                const int i = L.row(ri);
+                gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            }
+        } else {
+            // ----------------------------- phase 2, column panel tile (I, rn)
+            // A is the tile's transpose: the consumers write it into the A
+            // halves of the four ring stages this item uses, then run the
+            // product over B slabs (P).
+            mask_outside(acc, L, row0, col0, n);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);
+            consumer_barrier();  // every warp is done with the stages' previous use
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+                const int k = L.col(ci);
+                T* Ast = reinterpret_cast<T*>(ring + ((g + k / KS) % FZ_STAGES) * FZ_STAGE) + (k % KS) * TB;
+                vstore4(Ast + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+                vstore4(Ast + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+            }
+            // these stages are refilled by TMA later: order these writes first
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            consumer_barrier();
+            for (int s = 0; s < TB / KS; ++s, ++g) {
+                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
+                if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
+                const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
+                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
+            T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                const int i = L.row(ri);
+                gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            }
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+                const int k = L.col(ci);
+                vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+                vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+            }
+        }
+    }
+}
+
+}  // namespace apsp

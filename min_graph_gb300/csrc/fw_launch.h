@@ -33,14 +33,51 @@ struct RoundArgs {
     CUtensorMap tm_b;   // rowp,  TB x npad, box KS x TB
 };
 
+// Tensor maps and buffers of the round-fused schedule (fw_fused.cuh).
+struct FusedMaps {
+    CUtensorMap c;          // D: n x n, box TB x TB
+    CUtensorMap rowp[2];    // row panel buffers (alternate rounds): TB x npad, box KS x TB
+    CUtensorMap colpT[2];   // transposed column panel buffers
+    CUtensorMap prim;       // closed primary tile TB x TB, box KS x TB
+    CUtensorMap primT;      // its transpose
+};
+
+struct FusedPtrs {
+    void* rowp[2];
+    void* colpT[2];
+    void* prim;
+    void* primT;
+    int* flag_diag;   // [1]   round-stamped completion flags
+    int* flag_p1;     // [1]
+    int* flag_row;    // [nb]
+    int* flag_col;    // [nb]
+    int* counters;    // [nb + 1]: item counter of launch r at index r + 1
+    int* err;
+};
+
+struct FusedArgs {
+    void* d;
+    long long ld;
+    int n, nb, npad, sms;
+    unsigned long long timeout_ns;
+    int inject;     // test hook: withhold one k-slab in this launch (forces a timeout)
+    FusedMaps maps;
+    FusedPtrs ptrs;
+};
+
 // Opt the kernels into their shared-memory sizes on the current device.
 template <typename T> cudaError_t kernels_init();
 template <typename T> cudaError_t launch_phase1(const RoundArgs& a, int r, cudaStream_t s);
 template <typename T> cudaError_t launch_phase2(const RoundArgs& a, int r, cudaStream_t s);
 template <typename T> cudaError_t launch_phase3(const RoundArgs& a, int r, cudaStream_t s);
 
-// Bytes of workspace the round driver needs for n vertices (panels, primary
-// tiles, and the device error word at the end).
+// Launch r of the round-fused schedule (r = -1: prologue).  Returns
+// cudaSuccess without launching when the launch has no work items.
+template <typename T> cudaError_t launch_fused(const FusedArgs& a, int r, cudaStream_t s);
+
+// Bytes of workspace the round driver needs for n vertices: the device
+// error word, the panels and primary tiles of the three-kernel schedule,
+// then the second panel buffers, flags and counters of the fused schedule.
 size_t workspace_bytes(int n);
 
 // k-slab depth of the persistent phase 3 (the panel tensor maps' box height).

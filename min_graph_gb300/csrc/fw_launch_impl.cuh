@@ -2,6 +2,7 @@
 // fw_i32.cu and fw_f32.cu so that the two instantiations compile in parallel.
 #pragma once
 
+#include "fw_fused.cuh"
 #include "fw_kernels.cuh"
 #include "fw_launch.h"
 
@@ -22,8 +23,22 @@ cudaError_t kernels_init_impl() {
     e = cudaFuncSetAttribute(fw_phase3_persistent<T, 8, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)phase3p_smem(5));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(fw_phase3_persistent<T, 4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)phase3p_smem(4));
+    e = cudaFuncSetAttribute(fw_phase3_persistent<T, 4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)phase3p_smem(4));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fw_round_fused<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kFusedSmem);
+}
+
+template <typename T>
+cudaError_t launch_fused_impl(const FusedArgs& a, int r, cudaStream_t s) {
+    const long long items = fused_items(r, a.nb);
+    if (items <= 0) return cudaSuccess;
+    const int grid = (int)(items < a.sms ? items : a.sms);
+    fw_round_fused<T><<<grid, FZ_THREADS, kFusedSmem, s>>>(static_cast<T*>(a.d), a.ld, a.n, r, a.nb,
+                                                           a.npad, (int)items, a.maps, a.ptrs,
+                                                           a.timeout_ns, a.inject);
+    return cudaGetLastError();
 }
 
 template <typename T>
@@ -82,5 +97,8 @@ cudaError_t launch_phase3_impl(const RoundArgs& a, int r, cudaStream_t s) {
     }                                                                                            \
     template <> cudaError_t launch_phase3<T>(const RoundArgs& a, int r, cudaStream_t s) {        \
         return launch_phase3_impl<T>(a, r, s);                                                   \
+    }                                                                                            \
+    template <> cudaError_t launch_fused<T>(const FusedArgs& a, int r, cudaStream_t s) {         \
+        return launch_fused_impl<T>(a, r, s);                                                    \
     }                                                                                            \
     }

@@ -187,7 +187,9 @@ def test_validator_flags():
     assert apsp.validate(f) == 4
 
 
-def test_phase_timing_counts_launches():
+@pytest.mark.parametrize("fused", ["1", "0"])
+def test_phase_timing_counts_launches(fused, monkeypatch):
+    monkeypatch.setenv("APSP_FUSED", fused)
     w = torch.from_numpy(graphgen.er_i32(1000, 0.02, 1, 100, seed=4)).cuda()
     apsp.phase_timing_read()
     apsp.phase_timing_enable(True)
@@ -197,7 +199,11 @@ def test_phase_timing_counts_launches():
     finally:
         apsp.phase_timing_enable(False)
     nb = -(-1000 // apsp.TILE)
-    assert cnt == [nb, nb, nb]
+    if fused == "1":
+        assert cnt == [0, 0, nb + 1]  # prologue + one launch per round
+        ms = ms[2:]
+    else:
+        assert cnt == [nb, nb, nb]
     assert all(m > 0 for m in ms)
 
 
@@ -220,25 +226,49 @@ def test_empty_and_single():
     apsp.solve(t)
 
 
-PHASE3_VARIANTS = [("APSP_PHASE3", "cpasync"), ("APSP_P3_COLS", "8"), ("APSP_P3_COLS", "4")]
+# Environment settings that select each schedule / phase-3 kernel.
+PHASE3_VARIANTS = [
+    {},                                                # round-fused schedule (default)
+    {"APSP_FUSED": "0", "APSP_P3_COLS": "8"},          # three kernels, persistent phase 3
+    {"APSP_FUSED": "0", "APSP_P3_COLS": "4"},          # ... with 512 consumer threads
+    {"APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},     # ... with the cp.async phase 3
+]
 
 
-@pytest.mark.parametrize("n", [129, 300, 1000, 2100])
-def test_all_phase3_kernels_agree(n, monkeypatch):
-    """Every phase-3 kernel gives the oracle's result: the persistent TMA
-    kernel with 256 or 512 consumer threads, and the one-CTA-per-tile
-    cp.async kernel."""
+@pytest.mark.parametrize("n", [129, 255, 256, 300, 1000, 2100])
+def test_all_schedules_and_phase3_kernels_agree(n, monkeypatch):
+    """Every schedule and phase-3 kernel gives the oracle's result: the
+    round-fused schedule, and the three-kernel schedule with each phase-3
+    kernel."""
     w = graphgen.er_i32(n, 0.02, 1, 1000, seed=n + 7)
     ref = oracle.fw_i32(w, threads=threads())
     wf = graphgen.er_f32(n, 0.02, seed=n + 8)
     reff = oracle.fw_f64(wf, threads=threads())
-    for var, val in PHASE3_VARIANTS:
-        monkeypatch.setenv(var, val)
+    for env in PHASE3_VARIANTS:
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
         got, _ = gpu_solve(w)
         gotf, _ = gpu_solve(wf)
-        monkeypatch.delenv(var)
-        assert_i32_exact(got, ref, f"{var}={val}")
-        assert_f32_close(gotf, reff, f"{var}={val} f32")
+        for k in env:
+            monkeypatch.delenv(k)
+        assert_i32_exact(got, ref, f"{env}")
+        assert_f32_close(gotf, reff, f"{env} f32")
+
+
+@pytest.mark.parametrize("fused", ["1", "0"])
+def test_bounded_wait_timeout_each_schedule(fused, monkeypatch):
+    """The timeout hook works in both schedules."""
+    monkeypatch.setenv("APSP_FUSED", fused)
+    w = graphgen.er_i32(600, 0.02, 1, 100, seed=13)
+    t = torch.from_numpy(w).cuda()
+    apsp.stream_check()
+    apsp.debug_inject_phase3_timeout(50_000_000)
+    apsp.solve(t)
+    with pytest.raises(apsp.ApspError) as ei:
+        apsp.stream_check()
+    assert ei.value.status == apsp.ETIMEOUT
+    got, _ = gpu_solve(w)
+    assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), f"after timeout, fused={fused}")
 
 
 def test_bounded_wait_timeout_is_reported_and_context_survives():
