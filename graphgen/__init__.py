@@ -62,6 +62,8 @@ def _load():
             lib.graphgen_er_i32.restype = None
             lib.graphgen_er_f32.argtypes = [vp, i64, i64, i64, i64, dbl, u64]
             lib.graphgen_er_f32.restype = None
+            lib.graphgen_er_potential_i32.argtypes = [vp, i64, i64, i64, i64, dbl, i32, i32, i32, i32, u64]
+            lib.graphgen_er_potential_i32.restype = None
             lib.graphgen_ba_edges.argtypes = [vp, i64, i32, u64]
             lib.graphgen_ba_edges.restype = i64
             lib.graphgen_ba_i32.argtypes = [vp, i64, i64, i32, i32, i32, i32, u64]
@@ -121,6 +123,25 @@ def er_f32(n: int, p: float, seed: int, ld: int | None = None, out: np.ndarray |
 
     def rows(b, e):
         lib.graphgen_er_f32(base + b * ld * 4, n, ld, b, e, p, seed)
+
+    _rows_parallel(rows, n, threads)
+    return out
+
+
+def er_potential_i32(n: int, p: float, wlo: int, whi: int, pmax: int, seed: int,
+                     ld: int | None = None, out: np.ndarray | None = None, inf: int = INF_I32,
+                     threads: int | None = None) -> np.ndarray:
+    """Directed ER graph with negative arc weights but no negative cycle:
+    w(i, j) = w0(i, j) + p(i) - p(j), w0 uniform in [wlo, whi] (wlo >= 0),
+    vertex potentials p uniform in [0, pmax]."""
+    if wlo < 0:
+        raise ValueError("wlo must be >= 0")
+    out, ld = _alloc(n, ld, np.int32, out)
+    lib = _load()
+    base = out.ctypes.data
+
+    def rows(b, e):
+        lib.graphgen_er_potential_i32(base + b * ld * 4, n, ld, b, e, p, wlo, whi, pmax, inf, seed)
 
     _rows_parallel(rows, n, threads)
     return out

@@ -154,3 +154,28 @@ int64_t graphgen_ba_i32(int32_t* out, int64_t n, int64_t ld, int32_t beta, int32
     free(edges);
     return 2 * m;
 }
+
+/* Directed ER graph with some negative arc weights but no negative cycle:
+ * w(i, j) = w0(i, j) + p(i) - p(j), where w0 is uniform in [wlo, whi]
+ * (wlo >= 0) and p is a vertex potential uniform in [0, pmax] drawn at stream
+ * position 2^41 + i.  Every cycle's weight is the sum of its w0 >= 0.
+ * Presence and w0 use the same stream positions as graphgen_er_i32. */
+void graphgen_er_potential_i32(int32_t* out, int64_t n, int64_t ld, int64_t row_begin,
+                               int64_t row_end, double p, int32_t wlo, int32_t whi, int32_t pmax,
+                               int32_t inf, uint64_t seed) {
+    const uint64_t pbase = 1ULL << 41;
+    for (int64_t i = row_begin; i < row_end; ++i) {
+        int32_t* row = out + (i - row_begin) * ld;
+        const int32_t pi = gen_int(graphgen_splitmix64_at(seed, pbase + (uint64_t)i), 0, pmax);
+        for (int64_t j = 0; j < n; ++j) {
+            if (i == j) { row[j] = 0; continue; }
+            uint64_t t = 2u * (uint64_t)(i * n + j) + 1u;
+            if (gen_unit(graphgen_splitmix64_at(seed, t)) < p) {
+                const int32_t pj = gen_int(graphgen_splitmix64_at(seed, pbase + (uint64_t)j), 0, pmax);
+                row[j] = gen_int(graphgen_splitmix64_at(seed, t + 1u), wlo, whi) + pi - pj;
+            } else {
+                row[j] = inf;
+            }
+        }
+    }
+}

@@ -15,6 +15,10 @@ diagonal.  Two independent algorithms give it:
                            page, CEUR Vol-1631, the sequential Dijkstra
                            operators); reverse=True gives columns.
   bfs_hops_i32             reachability / hop counts.
+  bellman_ford_i32         single-source Bellman-Ford with the negative-cycle
+                           check (Johnson/Dijkstra page).
+  johnson_i32              Johnson's APSP as that page lays it out: negative
+                           arc weights allowed, negative cycles reported.
 
 int32 matrices use INF = 0x3FFFFFFF; floating point is computed in double
 with +inf for "no arc".
@@ -79,6 +83,10 @@ def bind(path: str):
     lib.oracle_dijkstra_f32.restype = i32
     lib.oracle_bfs_hops_i32.argtypes = [vp, i64, i64, i64, vp]
     lib.oracle_bfs_hops_i32.restype = i32
+    lib.oracle_bellman_ford_i32.argtypes = [vp, i64, i64, i64, vp]
+    lib.oracle_bellman_ford_i32.restype = i32
+    lib.oracle_johnson_i32.argtypes = [vp, i64, i64, vp, i32]
+    lib.oracle_johnson_i32.restype = i32
     return lib
 
 
@@ -167,6 +175,30 @@ class Oracle:
                                             threads or default_threads()), "dijkstra_f32")
         return out
 
+    def bellman_ford_i32(self, w: np.ndarray, src: int):
+        """Distances from src (int64, INF = 0x3FFFFFFF for unreachable), or
+        None when a negative cycle is reachable from src."""
+        w = _as_matrix(w, np.int32)
+        out = np.empty(w.shape[0], dtype=np.int64)
+        rc = self.lib.oracle_bellman_ford_i32(w.ctypes.data, w.shape[0], w.shape[1], src, out.ctypes.data)
+        if rc == 1:
+            return None
+        _check(rc, "bellman_ford_i32")
+        return out
+
+    def johnson_i32(self, w: np.ndarray, threads: int | None = None):
+        """All-pairs distances by Johnson's method (negative arc weights
+        allowed), int32 with INF; None when the graph has a negative cycle."""
+        w = _as_matrix(w, np.int32)
+        n = w.shape[0]
+        out = np.empty((n, n), dtype=np.int32)
+        rc = self.lib.oracle_johnson_i32(w.ctypes.data, n, w.shape[1], out.ctypes.data,
+                                         threads or default_threads())
+        if rc == 1:
+            return None
+        _check(rc, "johnson_i32")
+        return out
+
     def bfs_hops_i32(self, w: np.ndarray, src: int) -> np.ndarray:
         w = _as_matrix(w, np.int32)
         hops = np.empty(w.shape[0], dtype=np.int32)
@@ -203,3 +235,11 @@ def dijkstra_f32(w, sources, reverse=False, threads=None):
 
 def bfs_hops_i32(w, src):
     return default().bfs_hops_i32(w, src)
+
+
+def bellman_ford_i32(w, src):
+    return default().bellman_ford_i32(w, src)
+
+
+def johnson_i32(w, threads=None):
+    return default().johnson_i32(w, threads=threads)

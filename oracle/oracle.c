@@ -31,6 +31,15 @@
  *       ExtractMin and RelaxEdge).  reverse != 0 runs it on the reversed graph,
  *       which gives columns D[:, s] instead of rows.
  *   oracle_bfs_hops -- breadth-first hop counts (reachability).
+ *   oracle_bellman_ford_i32 -- single-source Bellman-Ford (Johnson/Dijkstra
+ *       page, the RelaxEdges/BellmanFord operators and the negative-cycle
+ *       condition cnc): |V| - 1 rounds relaxing every arc, stopping early when a
+ *       round changes nothing, then one more round to detect a negative cycle.
+ *   oracle_johnson_i32 -- Johnson's APSP as the same page lays it out: extend
+ *       the graph with a vertex s and 0-weight arcs s->v, Bellman-Ford from s
+ *       gives h, reweight w'(u,v) = w(u,v) + h(u) - h(v) >= 0, Dijkstra from
+ *       every vertex on w', and map back D(i,j) = D'(i,j) + h(j) - h(i).
+ *       Handles negative arc weights; reports a negative cycle.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -317,4 +326,99 @@ int oracle_bfs_hops_i32(const int32_t* w, int64_t n, int64_t ld, int64_t src, in
     }
     free(q);
     return 0;
+}
+
+/* ---------------- Bellman-Ford and Johnson ---------------- */
+
+/* Distances from src over arcs W[u][v] < INF (u != v), int64 arithmetic.
+ * out[v] = distance, or INF when v is unreachable.  Returns 0, or 1 when a
+ * negative cycle is reachable from src (out is then undefined), or < 0 on
+ * bad arguments. */
+int oracle_bellman_ford_i32(const int32_t* w, int64_t n, int64_t ld, int64_t src, int64_t* out) {
+    if (n <= 0 || ld < n || src < 0 || src >= n || !w || !out) return -1;
+    const int64_t UNSET = INT64_MAX;
+    for (int64_t v = 0; v < n; ++v) out[v] = UNSET;
+    out[src] = 0;
+    for (int64_t round = 0; round < n - 1; ++round) {        /* |V| - 1 rounds */
+        int changed = 0;
+        for (int64_t u = 0; u < n; ++u) {
+            if (out[u] == UNSET) continue;
+            for (int64_t v = 0; v < n; ++v) {
+                if (v == u || (int64_t)w[u * ld + v] >= O_INF) continue;
+                const int64_t nd = out[u] + w[u * ld + v];
+                if (nd < out[v]) { out[v] = nd; changed = 1; }
+            }
+        }
+        if (!changed) break;
+    }
+    for (int64_t u = 0; u < n; ++u) {                        /* cnc: any arc still relaxable? */
+        if (out[u] == UNSET) continue;
+        for (int64_t v = 0; v < n; ++v)
+            if (v != u && (int64_t)w[u * ld + v] < O_INF && out[u] + w[u * ld + v] < out[v]) return 1;
+    }
+    for (int64_t v = 0; v < n; ++v) if (out[v] == UNSET) out[v] = O_INF;
+    return 0;
+}
+
+/* All-pairs distances by Johnson's method.  out is n x n (int32, INF for
+ * unreachable).  Returns 0, 1 on a negative cycle, < 0 on bad arguments or
+ * allocation failure. */
+int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, int threads) {
+    if (n <= 0 || ld < n || !w || !out) return -1;
+    /* extendGraph + BellmanFord(s): s reaches every v directly with weight 0. */
+    int64_t* h = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+    if (!h) return -2;
+    for (int64_t v = 0; v < n; ++v) h[v] = 0;                /* after the arcs s->v */
+    h[n] = 0;                                                /* s itself */
+    for (int64_t round = 0; round < n; ++round) {            /* |V'| - 1 = n rounds */
+        int changed = 0;
+        for (int64_t u = 0; u < n; ++u)
+            for (int64_t v = 0; v < n; ++v) {
+                if (v == u || (int64_t)w[u * ld + v] >= O_INF) continue;
+                const int64_t nd = h[u] + w[u * ld + v];
+                if (nd < h[v]) { h[v] = nd; changed = 1; }
+            }
+        if (!changed) break;
+    }
+    for (int64_t u = 0; u < n; ++u)                          /* cnc */
+        for (int64_t v = 0; v < n; ++v)
+            if (v != u && (int64_t)w[u * ld + v] < O_INF && h[u] + w[u * ld + v] < h[v]) {
+                free(h);
+                return 1;
+            }
+    /* UpdateWeights: w'(u,v) = w(u,v) + h(u) - h(v), kept in the adjacency form */
+    o_graph g;
+    if (o_graph_build(&g, w, 0, n, ld, 0)) { free(h); return -2; }
+    for (int64_t u = 0; u < n; ++u)
+        for (int64_t e = g.off[u]; e < g.off[u + 1]; ++e) g.wi[e] += h[u] - h[g.dst[e]];
+    int err = 0;
+    (void)threads;
+#pragma omp parallel num_threads(threads > 0 ? threads : 1) if (threads > 1)
+    {
+        int64_t* di = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+        double* df = (double*)malloc(sizeof(double) * (size_t)n);
+        unsigned char* st = (unsigned char*)malloc((size_t)n);
+        if (!di || !df || !st) {
+#pragma omp atomic write
+            err = -2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < n; ++i) {
+                if (o_dijkstra_one(&g, i, 1, di, df, st)) {  /* D(i) on w' */
+#pragma omp atomic write
+                    err = -2;
+                    continue;
+                }
+                for (int64_t j = 0; j < n; ++j) {            /* to(): D(i,j) = D'(i,j) + h(j) - h(i) */
+                    if (di[j] == INT64_MAX) { out[i * n + j] = (int32_t)O_INF; continue; }
+                    const int64_t d = di[j] + h[j] - h[i];
+                    out[i * n + j] = (int32_t)(d < O_INF ? d : O_INF);
+                }
+            }
+        }
+        free(di); free(df); free(st);
+    }
+    o_graph_free(&g);
+    free(h);
+    return err;
 }

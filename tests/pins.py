@@ -25,13 +25,25 @@ GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 # ---------------------------------------------------------------- golden files
 
+def golden_flags(path: str) -> set:
+    """Flag lines of a fixture: 'negative' (negative arc weights, Dijkstra does
+    not apply), 'negative_cycle' (no distances exist; no D section)."""
+    flags = set()
+    with open(path) as f:
+        for line in f:
+            if line.strip() in ("negative", "negative_cycle"):
+                flags.add(line.strip())
+    return flags
+
+
 def load_golden(path: str):
-    """Parse a golden fixture: returns (name, dtype, W, D)."""
+    """Parse a golden fixture: returns (name, dtype, W, D); D is None for a
+    negative-cycle fixture."""
     dtype, n, mode, rows = None, None, None, {"W": [], "D": []}
     with open(path) as f:
         for line in f:
             line = line.strip()
-            if not line or line.startswith("#"):
+            if not line or line.startswith("#") or line in ("negative", "negative_cycle"):
                 continue
             if line.startswith("dtype"):
                 dtype = line.split()[1]
@@ -50,9 +62,12 @@ def load_golden(path: str):
 
     w = np.array([[conv(t) for t in r] for r in rows["W"]],
                  dtype=np.int64 if dtype == "int32" else np.float32)
-    d = np.array([[conv(t) for t in r] for r in rows["D"]],
-                 dtype=np.int64 if dtype == "int32" else np.float64)
-    assert w.shape == (n, n) and d.shape == (n, n)
+    d = None
+    if rows["D"]:
+        d = np.array([[conv(t) for t in r] for r in rows["D"]],
+                     dtype=np.int64 if dtype == "int32" else np.float64)
+        assert d.shape == (n, n)
+    assert w.shape == (n, n)
     if dtype == "int32":
         w = np.minimum(w, 2**31 - 1).astype(np.int32)
     return os.path.basename(path), dtype, w, d
@@ -67,6 +82,20 @@ def check_golden(orc) -> list[str]:
     for path in golden_files():
         name, dtype, w, d = load_golden(path)
         n = w.shape[0]
+        flags = golden_flags(path)
+        if "negative_cycle" in flags:
+            if orc.johnson_i32(w) is not None:
+                bad.append(f"golden {name}: Johnson missed the negative cycle")
+            if any(orc.bellman_ford_i32(w, s) is not None for s in range(n)):
+                bad.append(f"golden {name}: Bellman-Ford missed the negative cycle")
+            continue
+        if "negative" in flags:
+            outs = {"fw": orc.fw_i32(w), "johnson": orc.johnson_i32(w, threads=1)}
+            outs["bellman-ford"] = np.stack([orc.bellman_ford_i32(w, s) for s in range(n)])
+            for k, got in outs.items():
+                if got is None or not np.array_equal(np.asarray(got).astype(np.int64), d):
+                    bad.append(f"golden {name}: {k} differs")
+            continue
         if dtype == "int32":
             outs = {"fw": orc.fw_i32(w), "dijkstra": orc.dijkstra_i32(w, np.arange(n), threads=1),
                     "dijkstra-cols": orc.dijkstra_i32(w, np.arange(n), reverse=True, threads=1).T}
@@ -263,7 +292,47 @@ def check_fw_vs_dijkstra(orc) -> list[str]:
     return bad
 
 
-ALL_CHECKS = (check_golden, check_brute_force, check_closed_forms, check_invariants, check_fw_vs_dijkstra)
+def check_negative_weights(orc) -> list[str]:
+    """Negative arc weights without negative cycles: brute force over simple
+    paths (still the definition then), Floyd-Warshall, Johnson and
+    Bellman-Ford rows must all agree; a planted negative cycle is reported."""
+    bad = []
+    for seed in range(40):
+        rng = np.random.default_rng(500 + seed)
+        n = int(rng.integers(2, 8))
+        w = graphgen.er_potential_i32(n, float(rng.choice([0.3, 0.7])), 0, 20, 30, 500 + seed)
+        ref = brute_force(w, True)
+        jo = orc.johnson_i32(w, threads=1)
+        if jo is None or not np.array_equal(jo.astype(np.int64), ref):
+            bad.append(f"negative weights brute force seed {seed}: johnson differs")
+        if not np.array_equal(orc.fw_i32(w).astype(np.int64), ref):
+            bad.append(f"negative weights brute force seed {seed}: fw differs")
+        bf = np.stack([orc.bellman_ford_i32(w, s) for s in range(n)])
+        if not np.array_equal(bf, ref):
+            bad.append(f"negative weights brute force seed {seed}: bellman-ford differs")
+    for seed, (n, p) in enumerate([(150, 0.03), (200, 0.1), (64, 0.5)]):
+        w = graphgen.er_potential_i32(n, p, 0, 100, 400, 600 + seed)
+        fw = orc.fw_i32(w)
+        jo = orc.johnson_i32(w, threads=2)
+        if jo is None or not np.array_equal(fw, jo):
+            bad.append(f"negative weights seed {seed}: johnson != fw")
+        for s in (0, n // 2, n - 1):
+            bfr = orc.bellman_ford_i32(w, s)
+            if bfr is None or not np.array_equal(bfr, fw[s].astype(np.int64)):
+                bad.append(f"negative weights seed {seed}: bellman-ford row {s} != fw")
+        # plant a negative cycle: close a path with a very negative arc
+        w2 = w.copy()
+        w2[1, 2] = 0
+        w2[2, 1] = -1
+        if orc.johnson_i32(w2, threads=2) is not None:
+            bad.append(f"negative weights seed {seed}: planted negative cycle not reported")
+        if orc.bellman_ford_i32(w2, 1) is not None:
+            bad.append(f"negative weights seed {seed}: bellman-ford missed the planted cycle")
+    return bad
+
+
+ALL_CHECKS = (check_golden, check_brute_force, check_closed_forms, check_invariants, check_fw_vs_dijkstra,
+              check_negative_weights)
 
 
 def run_all(orc) -> list[str]:

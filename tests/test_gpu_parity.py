@@ -72,6 +72,8 @@ def test_entries_above_inf_read_as_inf():
 
 def test_golden_fixtures_on_gpu():
     for path in pins.golden_files():
+        if "negative" in pins.golden_flags(path):
+            continue  # the blocked FW contract is non-negative weights; the sparse path takes these
         name, dtype, w, d = pins.load_golden(path)
         got, _ = gpu_solve(w)
         if dtype == "int32":

@@ -20,7 +20,7 @@ def _fail_msg(bad):
 
 
 def test_golden_fixtures():
-    assert len(pins.golden_files()) >= 9
+    assert len(pins.golden_files()) >= 11
     bad = pins.check_golden(oracle.default())
     assert not bad, _fail_msg(bad)
 
@@ -42,6 +42,11 @@ def test_invariants():
 
 def test_fw_agrees_with_dijkstra():
     bad = pins.check_fw_vs_dijkstra(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_negative_weights():
+    bad = pins.check_negative_weights(oracle.default())
     assert not bad, _fail_msg(bad)
 
 
@@ -134,6 +139,14 @@ MUTANTS = [
      "double nd = df[u] + g->wf[e];", "double nd = g->wf[e];"),
     ("dijkstra: float weight read transposed",
      "g->wf[e] = (double)wf32[i * ld + j];", "g->wf[e] = (double)wf32[j * ld + i];"),
+    ("johnson: back-transform sign flipped",
+     "const int64_t d = di[j] + h[j] - h[i];", "const int64_t d = di[j] - h[j] + h[i];"),
+    ("johnson: reweighting sign flipped",
+     "g.wi[e] += h[u] - h[g.dst[e]];", "g.wi[e] += h[g.dst[e]] - h[u];"),
+    ("johnson: negative-cycle check disabled",
+     "h[u] + w[u * ld + v] < h[v]) {", "h[u] + w[u * ld + v] < h[v] - 2000000000) {"),
+    ("bellman-ford: source distance not zero",
+     "out[src] = 0;", "out[src] = 1;"),
 ]
 
 
