@@ -64,7 +64,8 @@ typedef enum {
     APSP_ECUDA = 2,         /* CUDA runtime/launch error; see apsp_last_cuda_error() */
     APSP_ETIMEOUT = 3,      /* a bounded device-side wait ran out */
     APSP_EUNSUPPORTED = 4,  /* current device is not compute capability 10.3 (sm_103a) */
-    APSP_ENOMEM = 5         /* workspace or staging allocation failed */
+    APSP_ENOMEM = 5,        /* workspace or staging allocation failed */
+    APSP_ENEGCYCLE = 6      /* the graph has a negative cycle (sparse entry points, apsp_sparse.h) */
 } apsp_status_t;
 
 #define APSP_INF_I32 0x3FFFFFFF

@@ -11,8 +11,12 @@ missing, every call raises.
     ...fill arcs, zero diagonal...
     apsp.solve(d)                 # in place, asynchronous on the current stream
 
-The functions mirror the C-ABI in include/apsp.h (same names without the
-apsp_ prefix).
+The functions mirror the C-ABI in include/apsp.h and include/apsp_sparse.h
+(same names without the apsp_ prefix).  The sparse entry points (Johnson's
+APSP with Delta-stepping searches) also take negative arc weights:
+
+    apsp.solve_sparse(d)          # in place, blocking; ApspError(ENEGCYCLE)
+                                  # when there is a negative cycle
 """
 from __future__ import annotations
 
@@ -24,7 +28,9 @@ INF_I32 = 0x3FFFFFFF
 TILE = 128
 MAX_N = 262144
 
-OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ENOMEM = range(6)
+SPARSE_MAX_N = 32768
+
+OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ENOMEM, ENEGCYCLE = range(7)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libapsp.so")
@@ -82,6 +88,18 @@ def load():
         lib.apsp_phase_timing_read.restype = i32
         lib.apsp_debug_inject_phase3_timeout.argtypes = [ctypes.c_ulonglong]
         lib.apsp_debug_inject_phase3_timeout.restype = i32
+        lib.apsp_solve_sparse_i32.argtypes = [vp, i32, i32, i32, vp]
+        lib.apsp_solve_sparse_i32.restype = i32
+        lib.apsp_johnson_csr_i32.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
+        lib.apsp_johnson_csr_i32.restype = i32
+        lib.apsp_sssp_delta_i32.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
+        lib.apsp_sssp_delta_i32.restype = i32
+        lib.apsp_csr_count_i32.argtypes = [vp, i32, i32, vp, ctypes.POINTER(i64), vp]
+        lib.apsp_csr_count_i32.restype = i32
+        lib.apsp_csr_fill_i32.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+        lib.apsp_csr_fill_i32.restype = i32
+        lib.apsp_sparse_release.argtypes = []
+        lib.apsp_sparse_release.restype = i32
         _lib = lib
         return lib
 
@@ -226,3 +244,111 @@ def debug_inject_phase3_timeout(timeout_ns: int) -> None:
     persistent phase 3 skips one k-slab, so a bounded device wait runs out
     after `timeout_ns` and the next stream_check raises ApspError(ETIMEOUT)."""
     _check(load().apsp_debug_inject_phase3_timeout(int(timeout_ns)), "apsp_debug_inject_phase3_timeout")
+
+
+# ---------------------------------------------------------------- sparse path
+
+
+def _i32_matrix(t):
+    import torch
+
+    ptr, n, ld = _matrix_args(t)
+    if t.dtype != torch.int32:
+        raise TypeError("dtype must be int32")
+    return ptr, n, ld
+
+
+def _csr_args(row_ptr, col_idx, w):
+    import torch
+
+    if row_ptr.dtype != torch.int64 or col_idx.dtype != torch.int32 or w.dtype != torch.int32:
+        raise TypeError("CSR arrays must be int64 row_ptr, int32 col_idx, int32 w")
+    for a in (row_ptr, col_idx, w):
+        if not a.is_cuda or a.dim() != 1 or not a.is_contiguous():
+            raise ValueError("CSR arrays must be contiguous 1-D CUDA tensors")
+    if col_idx.numel() != w.numel():
+        raise ValueError("col_idx and w differ in length")
+    return int(row_ptr.numel()) - 1
+
+
+def solve_sparse(t, delta: int = 0, stream=None):
+    """In-place APSP on a square int32 CUDA tensor by Johnson's method with
+    Delta-stepping searches (include/apsp_sparse.h).  Negative arc weights
+    are allowed; a negative cycle raises ApspError with status ENEGCYCLE and
+    leaves t unchanged.  Blocks until done.  Returns t."""
+    import torch
+
+    lib = load()
+    ptr, n, ld = _i32_matrix(t)
+    s = _stream_handle(t, stream)
+    with torch.cuda.device(t.device):
+        _check(lib.apsp_solve_sparse_i32(ptr, n, ld, int(delta), s), "apsp_solve_sparse_i32")
+    return t
+
+
+def csr_from_dense(t, stream=None):
+    """(row_ptr int64[n+1], col_idx int32[m], w int32[m]) of a dense int32
+    CUDA matrix: arcs are the off-diagonal entries below INF."""
+    import torch
+
+    lib = load()
+    ptr, n, ld = _i32_matrix(t)
+    s = _stream_handle(t, stream)
+    row_ptr = torch.empty(n + 1, dtype=torch.int64, device=t.device)
+    m = ctypes.c_longlong(0)
+    with torch.cuda.device(t.device):
+        _check(lib.apsp_csr_count_i32(ptr, n, ld, row_ptr.data_ptr(), ctypes.byref(m), s),
+               "apsp_csr_count_i32")
+        # at least one element each, so that the pointers are valid even when m = 0
+        col = torch.empty(max(1, m.value), dtype=torch.int32, device=t.device)
+        w = torch.empty(max(1, m.value), dtype=torch.int32, device=t.device)
+        _check(lib.apsp_csr_fill_i32(ptr, n, ld, row_ptr.data_ptr(), col.data_ptr(), w.data_ptr(), s),
+               "apsp_csr_fill_i32")
+    return row_ptr, col[:m.value], w[:m.value]
+
+
+def johnson_csr(row_ptr, col_idx, w, delta: int = 0, out=None, stream=None):
+    """All-pairs distances of a CSR graph (Johnson's method) into an n x n
+    int32 CUDA tensor (`out`, or a new one).  Blocks until done."""
+    import torch
+
+    lib = load()
+    n = _csr_args(row_ptr, col_idx, w)
+    if out is None:
+        out = torch.empty((n, n), dtype=torch.int32, device=row_ptr.device)
+    optr, on, old = _i32_matrix(out)
+    if on != n:
+        raise ValueError("out must be n x n")
+    s = _stream_handle(row_ptr, stream)
+    with torch.cuda.device(row_ptr.device):
+        _check(lib.apsp_johnson_csr_i32(row_ptr.data_ptr(), col_idx.data_ptr(), w.data_ptr(), n,
+                                        int(delta), optr, old, s), "apsp_johnson_csr_i32")
+    return out
+
+
+def sssp_delta(row_ptr, col_idx, w, sources, delta: int = 0, out=None, stream=None):
+    """Delta-stepping from each source (int32 CUDA tensor) on a CSR graph
+    with weights >= 0.  Returns (or fills) an nsrc x n int32 tensor whose
+    row q is the distance vector of sources[q].  Blocks until done."""
+    import torch
+
+    lib = load()
+    n = _csr_args(row_ptr, col_idx, w)
+    if sources.dtype != torch.int32 or not sources.is_cuda or sources.dim() != 1 or not sources.is_contiguous():
+        raise ValueError("sources must be a contiguous 1-D int32 CUDA tensor")
+    nsrc = int(sources.numel())
+    if out is None:
+        out = torch.empty((nsrc, n), dtype=torch.int32, device=row_ptr.device)
+    if out.dtype != torch.int32 or out.dim() != 2 or out.shape != (nsrc, n) or (n > 1 and out.stride(1) != 1):
+        raise ValueError("out must be a row-major nsrc x n int32 tensor")
+    ldo = int(out.stride(0)) if nsrc > 1 else max(1, n)
+    s = _stream_handle(row_ptr, stream)
+    with torch.cuda.device(row_ptr.device):
+        _check(lib.apsp_sssp_delta_i32(row_ptr.data_ptr(), col_idx.data_ptr(), w.data_ptr(), n,
+                                       sources.data_ptr(), nsrc, int(delta), out.data_ptr(), ldo, s),
+               "apsp_sssp_delta_i32")
+    return out
+
+
+def sparse_release() -> None:
+    _check(load().apsp_sparse_release(), "apsp_sparse_release")

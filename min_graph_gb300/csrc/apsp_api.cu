@@ -479,6 +479,9 @@ apsp_status_t validate(const T* d, int n, int ld, cudaStream_t s, int* flags) {
 }  // namespace
 
 namespace apsp {
+// Lets the sparse entry points report through apsp_last_cuda_error().
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 size_t workspace_bytes(int n) {
     const size_t nb = (size_t)(n + kTB - 1) / kTB;
     const size_t npad = nb * kTB;
@@ -553,6 +556,7 @@ const char* apsp_status_string(apsp_status_t status) {
         case APSP_ETIMEOUT: return "APSP_ETIMEOUT: device-side wait timed out";
         case APSP_EUNSUPPORTED: return "APSP_EUNSUPPORTED: device is not sm_103";
         case APSP_ENOMEM: return "APSP_ENOMEM: device allocation failed";
+        case APSP_ENEGCYCLE: return "APSP_ENEGCYCLE: negative cycle";
     }
     return "unknown apsp status";
 }

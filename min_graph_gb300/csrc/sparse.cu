@@ -1,0 +1,727 @@
+// Sparse-graph shortest paths on sm_103a: Delta-stepping SSSP and Johnson's
+// APSP.  The contract is in include/apsp_sparse.h.
+//
+// Delta-stepping (Delta-stepping page, CEUR Vol-1662 comp2): one CTA runs
+// one source at a time.  Persistent CTAs take sources from a global counter.
+// The tentative distances, the "queued" set (vertices waiting in some
+// bucket), the set R (vertices removed from the current bucket) and the
+// frontier list all live in shared memory.  The bucket of a queued vertex is
+// dist / Delta, so no bucket arrays are kept.  The lowest non-empty bucket is
+// found by a scan of the queued bitmap.  A phase takes that bucket's queued
+// vertices as the frontier and relaxes their light arcs.  Vertices that
+// improve are queued again, and phases repeat until the bucket stays empty.
+// The heavy arcs of R are then relaxed once.  One warp walks one frontier
+// vertex's arc list, so a hub of a scale-free graph spreads over 32 lanes.
+// No step waits on another CTA: every loop ends because distances only
+// decrease.
+//
+// Johnson (Johnson/Dijkstra page, CEUR Vol-1631): Bellman-Ford from the
+// virtual vertex in int64, one launch per round, Gauss-Seidel style (a
+// round may use values updated in the same round, which only speeds
+// convergence).  It ends after a round that changes nothing; a change in
+// round n + 1 means a negative cycle.  Then the reweighting
+// w' = w + h(u) - h(v), the searches on w', and the mapping back in each
+// search's epilogue.
+//
+// Arithmetic: distances in the search are int32 with INT_MAX as
+// "unreached".  A relaxation adds in unsigned 32-bit arithmetic (both terms
+// are below 2^31, so the sum cannot wrap) and saturates at INT_MAX.  With
+// h > -INF, every reweighted distance of a pair whose true distance is below
+// INF is below 2 * INF < INT_MAX.  So those come out exact, and the rest map
+// to INF.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/apsp.h"
+#include "../../include/apsp_sparse.h"
+
+namespace apsp {
+void set_last_cuda_error(int e);  // defined with apsp_last_cuda_error()
+}
+
+namespace {
+
+constexpr int32_t kInf = APSP_INF_I32;
+constexpr int32_t kUnreached = INT_MAX;
+constexpr int kSpThreads = 512;
+constexpr int kSpWarps = kSpThreads / 32;
+constexpr int kScanThreads = 1024;
+
+apsp_status_t sp_fail(cudaError_t e) {
+    apsp::set_last_cuda_error((int)e);
+    return APSP_ECUDA;
+}
+
+bool sp_supported_device() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3;
+}
+
+// ------------------------------------------------------------------ CSR build
+
+// Arcs per row (warp per row); row_ptr[row + 1] = count, row_ptr[0] = 0.
+__global__ void csr_count_kernel(const int32_t* __restrict__ d, long long ld, int n,
+                                 int64_t* __restrict__ rp) {
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= n) return;
+    const int row = (int)wid;
+    const int32_t* drow = d + (long long)row * ld;
+    int cnt = 0;
+    for (int j = lane; j < n; j += 32) cnt += (j != row && drow[j] < kInf) ? 1 : 0;
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) {
+        rp[row + 1] = cnt;
+        if (row == 0) rp[0] = 0;
+    }
+}
+
+// In-place inclusive prefix sum of a[1..n] (a[0] = 0) by one CTA: each
+// thread sums a contiguous chunk, the chunk sums are scanned in shared
+// memory, and each thread rewrites its chunk.
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(int64_t* __restrict__ a, int n) {
+    __shared__ int64_t part[kScanThreads];
+    const int t = threadIdx.x;
+    const int chunk = (n + kScanThreads - 1) / kScanThreads;
+    const int b = 1 + t * chunk, e = min(n + 1, b + chunk);
+    int64_t s = 0;
+    for (int i = b; i < e; ++i) s += a[i];
+    part[t] = s;
+    __syncthreads();
+    for (int off = 1; off < kScanThreads; off <<= 1) {
+        const int64_t v = t >= off ? part[t - off] : 0;
+        __syncthreads();
+        part[t] += v;
+        __syncthreads();
+    }
+    int64_t run = t > 0 ? part[t - 1] : 0;
+    for (int i = b; i < e; ++i) {
+        run += a[i];
+        a[i] = run;
+    }
+}
+
+// Column indices and weights of each row, in column order (warp per row;
+// a ballot gives each arc its slot).
+__global__ void csr_fill_kernel(const int32_t* __restrict__ d, long long ld, int n,
+                                const int64_t* __restrict__ rp, int32_t* __restrict__ col,
+                                int32_t* __restrict__ w) {
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= n) return;
+    const int row = (int)wid;
+    const int32_t* drow = d + (long long)row * ld;
+    int64_t pos = rp[row];
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        const int j = j0 + lane;
+        const int32_t v = j < n ? drow[j] : kInf;
+        const bool arc = j < n && j != row && v < kInf;
+        const unsigned mask = __ballot_sync(0xffffffffu, arc);
+        if (arc) {
+            const int64_t p = pos + __popc(mask & ((1u << lane) - 1u));
+            col[p] = j;
+            w[p] = v;
+        }
+        pos += __popc(mask);
+    }
+}
+
+// min and max of w[0..m) into range[0], range[1], and whether any head
+// col[e] lies outside [0, n) into range[2] (initialised INT_MAX, INT_MIN, 0).
+__global__ void weight_range_kernel(const int32_t* __restrict__ w, const int32_t* __restrict__ col,
+                                    long long m, int n, int* __restrict__ range) {
+    int lo = INT_MAX, hi = INT_MIN;
+    unsigned bad = 0;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < m;
+         e += (long long)gridDim.x * blockDim.x) {
+        lo = min(lo, w[e]);
+        hi = max(hi, w[e]);
+        if (col) bad |= (unsigned)col[e] >= (unsigned)n ? 1u : 0u;
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if ((threadIdx.x & 31) == 0) {
+        atomicMin(range, lo);
+        atomicMax(range + 1, hi);
+        if (bad) atomicOr(range + 2, 1);
+    }
+}
+
+// *bad = 1 unless row_ptr[0] = 0 and row_ptr is non-decreasing.
+__global__ void rowptr_check_kernel(const int64_t* __restrict__ rp, int n, int* __restrict__ bad) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i > n) return;
+    if (i == 0 ? rp[0] != 0 : rp[i] < rp[i - 1]) atomicOr(bad, 1);
+}
+
+// ------------------------------------------------------------------ Bellman-Ford
+
+// One round over every arc against the potentials h (warp per tail vertex).
+__global__ void bf_round_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                                const int32_t* __restrict__ w, int n, long long* __restrict__ h,
+                                int* __restrict__ changed) {
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= n) return;
+    const int u = (int)wid;
+    const long long hu = *reinterpret_cast<volatile long long*>(h + u);
+    int any = 0;
+    for (int64_t e = rp[u] + lane; e < rp[u + 1]; e += 32) {
+        const int v = col[e];
+        const long long nv = hu + w[e];
+        if (nv < *reinterpret_cast<volatile long long*>(h + v) && nv < atomicMin(h + v, nv)) any = 1;
+    }
+    if (__any_sync(0xffffffffu, any) && lane == 0) *changed = 1;
+}
+
+// w' = w + h(u) - h(v) (>= 0 once Bellman-Ford has converged).  flag gets 1
+// when some h(u) <= -INF: a distance below the int32 range.
+__global__ void reweight_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                                const int32_t* __restrict__ w, int n, const long long* __restrict__ h,
+                                int32_t* __restrict__ wh, int* __restrict__ flag) {
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= n) return;
+    const int u = (int)wid;
+    const long long hu = h[u];
+    if (hu <= -(long long)kInf) {
+        if (lane == 0) *flag = 1;
+        return;
+    }
+    for (int64_t e = rp[u] + lane; e < rp[u + 1]; e += 32) {
+        const long long hv = h[col[e]];
+        // hv > -INF (checked by v's own warp), hu <= 0, w < INF: 0 <= w' < 2 * INF
+        wh[e] = (int32_t)((long long)w[e] + hu - (hv > -(long long)kInf ? hv : 0));
+    }
+}
+
+// ------------------------------------------------------------------ Delta-stepping
+
+struct SpShared {
+    int qlen;
+    int bmin;
+    int item;
+};
+
+__host__ __device__ constexpr size_t sssp_shared_offset(int n) {
+    return ((size_t)n * 4 + (size_t)((n + 31) / 32) * 8 + (size_t)n * 2 + 15) / 16 * 16;
+}
+
+size_t sssp_smem_bytes(int n) { return sssp_shared_offset(n) + sizeof(SpShared); }
+
+// Relax the arcs of frontier vertices queue[0..qlen) whose weight is light
+// (kLight) or heavy (!kLight) against delta.
+template <bool kLight>
+__device__ __forceinline__ void relax_frontier(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                                               const int32_t* __restrict__ w, int32_t delta,
+                                               const uint16_t* queue, int qlen, int32_t* dist,
+                                               uint32_t* queued, int warp, int lane) {
+    for (int qi = warp; qi < qlen; qi += kSpWarps) {
+        const int v = queue[qi];
+        const uint32_t dv = (uint32_t)dist[v];
+        const int64_t e1 = rp[v + 1];
+        for (int64_t e = rp[v] + lane; e < e1; e += 32) {
+            const int32_t we = w[e];
+            if (kLight ? we > delta : we <= delta) continue;
+            const uint32_t s = dv + (uint32_t)we;  // < 2^32: both terms < 2^31
+            const int32_t nd = s >= (uint32_t)kUnreached ? kUnreached : (int32_t)s;
+            const int u = col[e];
+            if (nd < dist[u] && nd < atomicMin(dist + u, nd)) atomicOr(queued + (u >> 5), 1u << (u & 31));
+        }
+    }
+}
+
+// Append the members of `sel` (word i of a bitmap) to the frontier list.
+__device__ __forceinline__ void push_bits(uint32_t sel, int i, uint16_t* queue, int* qlen) {
+    int p = atomicAdd(qlen, __popc(sel));
+    while (sel) {
+        const int b = __ffs(sel) - 1;
+        sel &= sel - 1;
+        queue[p++] = (uint16_t)(i * 32 + b);
+    }
+}
+
+// Row `item` of out gets the distances from source sources[item] (or item
+// when sources is null).  With h non-null the search ran on reweighted arcs
+// and the epilogue maps back: out = dist + h[v] - h[src].  A source outside
+// [0, n) sets bit 0 of *err and its row is skipped.
+__global__ void __launch_bounds__(kSpThreads, 1)
+sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                  const int32_t* __restrict__ w, int n, const int32_t* __restrict__ sources, int nsrc,
+                  int32_t delta, const long long* __restrict__ h, int32_t* __restrict__ out, long long ldo,
+                  int* __restrict__ counter, int* __restrict__ err) {
+    extern __shared__ __align__(16) unsigned char sp_smem[];
+    const int nw = (n + 31) / 32;
+    int32_t* dist = reinterpret_cast<int32_t*>(sp_smem);
+    uint32_t* queued = reinterpret_cast<uint32_t*>(dist + n);
+    uint32_t* rset = queued + nw;
+    uint16_t* queue = reinterpret_cast<uint16_t*>(rset + nw);
+    SpShared* sh = reinterpret_cast<SpShared*>(sp_smem + sssp_shared_offset(n));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (;;) {
+        if (tid == 0) sh->item = atomicAdd(counter, 1);
+        __syncthreads();
+        const int item = sh->item;
+        __syncthreads();  // everyone has read sh->item before thread 0 may rewrite it
+        if (item >= nsrc) return;
+        const int src = sources ? sources[item] : item;
+        if (src < 0 || src >= n) {
+            if (tid == 0) atomicOr(err, 1);
+            continue;
+        }
+        for (int v = tid; v < n; v += kSpThreads) dist[v] = kUnreached;
+        for (int i = tid; i < nw; i += kSpThreads) {
+            queued[i] = 0u;
+            rset[i] = 0u;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            dist[src] = 0;
+            queued[src >> 5] = 1u << (src & 31);
+        }
+        __syncthreads();
+
+        for (;;) {
+            // the lowest non-empty bucket
+            if (tid == 0) sh->bmin = INT_MAX;
+            __syncthreads();
+            int local = INT_MAX;
+            for (int i = tid; i < nw; i += kSpThreads) {
+                uint32_t bits = queued[i];
+                while (bits) {
+                    const int b = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    local = min(local, dist[i * 32 + b] / delta);
+                }
+            }
+            local = __reduce_min_sync(0xffffffffu, local);
+            if (lane == 0 && local != INT_MAX) atomicMin(&sh->bmin, local);
+            __syncthreads();
+            const int bmin = sh->bmin;
+            if (bmin == INT_MAX) break;
+
+            // light phases until the bucket stays empty
+            for (;;) {
+                if (tid == 0) sh->qlen = 0;
+                __syncthreads();
+                for (int i = tid; i < nw; i += kSpThreads) {
+                    uint32_t bits = queued[i], sel = 0u;
+                    while (bits) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        if (dist[i * 32 + b] / delta == bmin) sel |= 1u << b;
+                    }
+                    if (sel) {
+                        queued[i] &= ~sel;
+                        rset[i] |= sel;
+                        push_bits(sel, i, queue, &sh->qlen);
+                    }
+                }
+                __syncthreads();
+                const int qlen = sh->qlen;
+                if (qlen == 0) break;
+                relax_frontier<true>(rp, col, w, delta, queue, qlen, dist, queued, warp, lane);
+                __syncthreads();
+            }
+
+            // heavy arcs of R, once
+            if (tid == 0) sh->qlen = 0;
+            __syncthreads();
+            for (int i = tid; i < nw; i += kSpThreads) {
+                const uint32_t sel = rset[i];
+                if (sel) {
+                    rset[i] = 0u;
+                    push_bits(sel, i, queue, &sh->qlen);
+                }
+            }
+            __syncthreads();
+            relax_frontier<false>(rp, col, w, delta, queue, sh->qlen, dist, queued, warp, lane);
+            __syncthreads();
+        }
+
+        int32_t* orow = out + (long long)item * ldo;
+        const long long hs = h ? h[src] : 0;
+        for (int v = tid; v < n; v += kSpThreads) {
+            const int32_t dv = dist[v];
+            long long r = dv;
+            if (h && dv != kUnreached) r = (long long)dv + h[v] - hs;
+            orow[v] = (dv == kUnreached || r >= kInf) ? kInf : (int32_t)r;
+        }
+        __syncthreads();  // the next source reuses shared memory
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct DevBuf {
+    void* p = nullptr;
+    size_t bytes = 0;
+};
+
+struct SparseState {
+    DevBuf rp, body, work;
+};
+
+std::mutex g_sp_mu;
+std::vector<SparseState> g_sp;
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+apsp_status_t grow(DevBuf& b, size_t need) {
+    if (b.bytes >= need) return APSP_OK;
+    if (b.p) {
+        cudaDeviceSynchronize();
+        cudaFree(b.p);
+        b.p = nullptr;
+        b.bytes = 0;
+    }
+    const cudaError_t e = cudaMalloc(&b.p, need);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        b.p = nullptr;
+        apsp::set_last_cuda_error((int)e);
+        return APSP_ENOMEM;
+    }
+    b.bytes = need;
+    return APSP_OK;
+}
+
+SparseState* sp_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if ((int)g_sp.size() <= dev) g_sp.resize(dev + 1);
+    return &g_sp[dev];
+}
+
+int blocks_for_warps(long long warps) { return (int)((warps * 32 + 255) / 256); }
+
+// work buffer: [0, 256) small counters, then h (int64 n), then w' (int32 m)
+struct Work {
+    int* range;    // [0] min, [1] max, [2] bad head
+    int* counter;  // source counter of the search
+    int* changed;  // Bellman-Ford round flag, then the reweighting range flag
+    int* err;      // search error bits
+    long long* h;
+    int32_t* wh;
+};
+
+size_t work_bytes(int n, long long m) {
+    return 256 + align256((size_t)n * 8) + align256((size_t)(m > 0 ? m : 1) * 4);
+}
+
+Work work_layout(void* base, int n) {
+    char* b = static_cast<char*>(base);
+    Work wk;
+    wk.range = reinterpret_cast<int*>(b);
+    wk.counter = wk.range + 4;
+    wk.changed = wk.range + 5;
+    wk.err = wk.range + 6;
+    wk.h = reinterpret_cast<long long*>(b + 256);
+    wk.wh = reinterpret_cast<int32_t*>(b + 256 + align256((size_t)n * 8));
+    return wk;
+}
+
+apsp_status_t read_int(const int* dev, int* host, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(host, dev, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? APSP_OK : sp_fail(e);
+}
+
+apsp_status_t read_m(const int64_t* rp, int n, long long* m, cudaStream_t s) {
+    int64_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, rp + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return sp_fail(e);
+    *m = (long long)v;
+    return APSP_OK;
+}
+
+// Weight range (and head check when col is given) of m arcs.
+apsp_status_t weight_range(const int32_t* w, const int32_t* col, long long m, int n, int* range,
+                           cudaStream_t s, int* lo, int* hi, int* bad) {
+    const int init[3] = {INT_MAX, INT_MIN, 0};
+    cudaError_t e = cudaMemcpyAsync(range, init, sizeof(init), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return sp_fail(e);
+    if (m > 0) {
+        long long blocks = (m + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        weight_range_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, col, m, n, range);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return sp_fail(e);
+    }
+    int r[3];
+    e = cudaMemcpyAsync(r, range, sizeof(r), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return sp_fail(e);
+    *lo = r[0];
+    *hi = r[1];
+    if (bad) *bad = r[2];
+    return APSP_OK;
+}
+
+// A caller's row_ptr: row_ptr[0] = 0 and non-decreasing (so every arc
+// index a search forms lies in [0, row_ptr[n])).
+apsp_status_t check_row_ptr(const int64_t* rp, int n, int* flag, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
+    if (e != cudaSuccess) return sp_fail(e);
+    rowptr_check_kernel<<<(n + 1 + 255) / 256, 256, 0, s>>>(rp, n, flag);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    int bad = 0;
+    apsp_status_t rc = read_int(flag, &bad, s);
+    if (rc != APSP_OK) return rc;
+    return bad ? APSP_EINVAL : APSP_OK;
+}
+
+// Bucket width when the caller gives none: the largest arc weight spread
+// over a few out-degrees, so that a bucket holds several hops of the
+// search front.
+int32_t default_delta(int n, long long m, int wmax) {
+    if (m <= 0 || wmax <= 0) return 1;
+    const double avg_deg = (double)m / (double)(n > 0 ? n : 1);
+    double d = 8.0 * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
+    if (d < 1.0) d = 1.0;
+    if (d > (double)kInf) d = (double)kInf;
+    return (int32_t)d;
+}
+
+apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, const int32_t* sources,
+                          int nsrc, int32_t delta, const long long* h, int32_t* out, long long ldo, const Work& wk,
+                          cudaStream_t s) {
+    const size_t smem = sssp_smem_bytes(n);
+    cudaError_t e = cudaFuncSetAttribute(sssp_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return sp_fail(e);
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel, kSpThreads, smem);
+    if (e != cudaSuccess) return sp_fail(e);
+    if (per_sm < 1) return APSP_EUNSUPPORTED;
+    long long grid = (long long)sms * per_sm;
+    if (grid > nsrc) grid = nsrc;
+    e = cudaMemsetAsync(wk.counter, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(wk.err, 0, sizeof(int), s);
+    if (e != cudaSuccess) return sp_fail(e);
+    sssp_delta_kernel<<<(unsigned)grid, kSpThreads, smem, s>>>(rp, col, w, n, sources, nsrc, delta, h, out, ldo,
+                                                               wk.counter, wk.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    int err = 0;
+    apsp_status_t rc = read_int(wk.err, &err, s);
+    if (rc != APSP_OK) return rc;
+    return err ? APSP_EINVAL : APSP_OK;
+}
+
+// Johnson's APSP on a device CSR with m arcs into out (n x ld).
+apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m, int32_t delta,
+                      int32_t* out, int ld, const Work& wk, bool check_heads, cudaStream_t s) {
+    int lo = 0, hi = 0, bad = 0;
+    apsp_status_t rc = weight_range(w, check_heads ? col : nullptr, m, n, wk.range, s, &lo, &hi, &bad);
+    if (rc != APSP_OK) return rc;
+    if (bad || (m > 0 && (lo <= -kInf || hi >= kInf))) return APSP_EINVAL;
+    const int32_t* wuse = w;
+    const long long* huse = nullptr;
+    cudaError_t e;
+    if (m > 0 && lo < 0) {
+        // Bellman-Ford from the virtual vertex s: its 0-weight arcs give h = 0.
+        e = cudaMemsetAsync(wk.h, 0, (size_t)n * 8, s);
+        if (e != cudaSuccess) return sp_fail(e);
+        bool converged = false;
+        for (int round = 0; round <= n; ++round) {  // n = |V'| - 1 rounds, then one more as the check
+            e = cudaMemsetAsync(wk.changed, 0, sizeof(int), s);
+            if (e != cudaSuccess) return sp_fail(e);
+            bf_round_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, wk.h, wk.changed);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return sp_fail(e);
+            int changed = 0;
+            rc = read_int(wk.changed, &changed, s);
+            if (rc != APSP_OK) return rc;
+            if (!changed) {
+                converged = true;
+                break;
+            }
+        }
+        if (!converged) return APSP_ENEGCYCLE;
+        e = cudaMemsetAsync(wk.changed, 0, sizeof(int), s);
+        if (e != cudaSuccess) return sp_fail(e);
+        reweight_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, wk.h, wk.wh, wk.changed);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return sp_fail(e);
+        int range_bad = 0;
+        rc = read_int(wk.changed, &range_bad, s);
+        if (rc != APSP_OK) return rc;
+        if (range_bad) return APSP_EINVAL;
+        wuse = wk.wh;
+        huse = wk.h;
+        rc = weight_range(wk.wh, nullptr, m, n, wk.range, s, &lo, &hi, nullptr);
+        if (rc != APSP_OK) return rc;
+    }
+    if (delta <= 0) delta = default_delta(n, m, hi);
+    return launch_sssp(rp, col, wuse, n, nullptr, n, delta, huse, out, ld, wk, s);
+}
+
+// CSR of a dense matrix into st.rp / st.body; returns m.
+apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, long long* m_out, cudaStream_t s) {
+    apsp_status_t rc = grow(st.rp, align256((size_t)(n + 1) * 8));
+    if (rc != APSP_OK) return rc;
+    int64_t* rp = static_cast<int64_t*>(st.rp.p);
+    csr_count_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, rp);
+    scan_kernel<<<1, kScanThreads, 0, s>>>(rp, n);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    long long m = 0;
+    rc = read_m(rp, n, &m, s);
+    if (rc != APSP_OK) return rc;
+    const size_t colb = align256((size_t)(m > 0 ? m : 1) * 4);
+    rc = grow(st.body, 2 * colb);
+    if (rc != APSP_OK) return rc;
+    int32_t* col = static_cast<int32_t*>(st.body.p);
+    int32_t* w = reinterpret_cast<int32_t*>(static_cast<char*>(st.body.p) + colb);
+    csr_fill_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, rp, col, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    *m_out = m;
+    return APSP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+apsp_status_t apsp_csr_count_i32(const int32_t* dist, int n, int ld, int64_t* row_ptr, long long* m_out,
+                                 apsp_stream_t stream) {
+    if (n < 0 || n > APSP_MAX_N || ld < n || row_ptr == nullptr || m_out == nullptr || (n > 0 && dist == nullptr))
+        return APSP_EINVAL;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    if (n == 0) {
+        const cudaError_t e = cudaMemsetAsync(row_ptr, 0, sizeof(int64_t), s);
+        if (e != cudaSuccess) return sp_fail(e);
+        *m_out = 0;
+        return APSP_OK;
+    }
+    csr_count_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, row_ptr);
+    scan_kernel<<<1, kScanThreads, 0, s>>>(row_ptr, n);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    return read_m(row_ptr, n, m_out, s);
+}
+
+apsp_status_t apsp_csr_fill_i32(const int32_t* dist, int n, int ld, const int64_t* row_ptr, int32_t* col_idx,
+                                int32_t* w, apsp_stream_t stream) {
+    if (n < 0 || n > APSP_MAX_N || ld < n ||
+        (n > 0 && (dist == nullptr || row_ptr == nullptr || col_idx == nullptr || w == nullptr)))
+        return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    csr_fill_kernel<<<blocks_for_warps(n), 256, 0, (cudaStream_t)stream>>>(dist, ld, n, row_ptr, col_idx, w);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    return APSP_OK;
+}
+
+apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
+                                  const int32_t* sources, int nsrc, int32_t delta, int32_t* out, int ldo,
+                                  apsp_stream_t stream) {
+    if (n < 0 || n > APSP_SPARSE_MAX_N || nsrc < 0 || ldo < n) return APSP_EINVAL;
+    if (n > 0 && nsrc > 0 && (row_ptr == nullptr || sources == nullptr || out == nullptr)) return APSP_EINVAL;
+    if (n == 0 || nsrc == 0) return APSP_OK;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    SparseState* st = sp_state();
+    if (!st) return APSP_ECUDA;
+    long long m = 0;
+    apsp_status_t rc = read_m(row_ptr, n, &m, s);
+    if (rc != APSP_OK) return rc;
+    if (m < 0 || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
+    rc = grow(st->work, 256);
+    if (rc != APSP_OK) return rc;
+    const Work wk = work_layout(st->work.p, 0);
+    rc = check_row_ptr(row_ptr, n, wk.err, s);
+    if (rc != APSP_OK) return rc;
+    int lo = 0, hi = 0, bad = 0;
+    rc = weight_range(w, col_idx, m, n, wk.range, s, &lo, &hi, &bad);
+    if (rc != APSP_OK) return rc;
+    if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
+    if (delta <= 0) delta = default_delta(n, m, hi);
+    return launch_sssp(row_ptr, col_idx, w, n, sources, nsrc, delta, nullptr, out, ldo, wk, s);
+}
+
+apsp_status_t apsp_johnson_csr_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
+                                   int32_t delta, int32_t* out, int ld, apsp_stream_t stream) {
+    if (n < 0 || n > APSP_SPARSE_MAX_N || ld < n || (n > 0 && (row_ptr == nullptr || out == nullptr)))
+        return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    SparseState* st = sp_state();
+    if (!st) return APSP_ECUDA;
+    long long m = 0;
+    apsp_status_t rc = read_m(row_ptr, n, &m, s);
+    if (rc != APSP_OK) return rc;
+    if (m < 0 || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
+    rc = grow(st->work, work_bytes(n, m));
+    if (rc != APSP_OK) return rc;
+    const Work wk = work_layout(st->work.p, n);
+    rc = check_row_ptr(row_ptr, n, wk.err, s);
+    if (rc != APSP_OK) return rc;
+    return johnson(row_ptr, col_idx, w, n, m, delta, out, ld, wk, true, s);
+}
+
+apsp_status_t apsp_solve_sparse_i32(int32_t* dist, int n, int ld, int32_t delta, apsp_stream_t stream) {
+    if (n < 0 || n > APSP_SPARSE_MAX_N || ld < n || (n > 0 && dist == nullptr)) return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    SparseState* st = sp_state();
+    if (!st) return APSP_ECUDA;
+    long long m = 0;
+    apsp_status_t rc = build_csr(dist, n, ld, *st, &m, s);
+    if (rc != APSP_OK) return rc;
+    rc = grow(st->work, work_bytes(n, m));
+    if (rc != APSP_OK) return rc;
+    const size_t colb = align256((size_t)(m > 0 ? m : 1) * 4);
+    const int64_t* rp = static_cast<const int64_t*>(st->rp.p);
+    const int32_t* col = static_cast<const int32_t*>(st->body.p);
+    const int32_t* w = reinterpret_cast<const int32_t*>(static_cast<const char*>(st->body.p) + colb);
+    // The searches read only the CSR, so they may overwrite dist as they go.
+    return johnson(rp, col, w, n, m, delta, dist, ld, work_layout(st->work.p, n), false, s);
+}
+
+apsp_status_t apsp_sparse_release(void) {
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    apsp_status_t rc = APSP_OK;
+    for (size_t dev = 0; dev < g_sp.size(); ++dev) {
+        SparseState& st = g_sp[dev];
+        if (!st.rp.p && !st.body.p && !st.work.p) continue;
+        if (cudaSetDevice((int)dev) != cudaSuccess) {
+            rc = APSP_ECUDA;
+            continue;
+        }
+        cudaDeviceSynchronize();
+        for (DevBuf* b : {&st.rp, &st.body, &st.work}) {
+            if (b->p) cudaFree(b->p);
+            b->p = nullptr;
+            b->bytes = 0;
+        }
+    }
+    cudaSetDevice(cur);
+    return rc;
+}
+
+}  // extern "C"

@@ -25,6 +25,7 @@ def declared_functions(header: str):
 
 
 @pytest.mark.parametrize("header,lib", [("apsp.h", "libapsp.so"), ("apsp_debug.h", "libapsp.so"),
+                                        ("apsp_sparse.h", "libapsp.so"),
                                         ("apsp_peak.h", "libapsp_peak.so")])
 def test_every_declared_symbol_is_exported(libs, header, lib):
     names = declared_functions(header)
@@ -40,11 +41,14 @@ def test_header_constants_match_binding():
     assert apsp.INF_I32 == 0x3FFFFFFF
     assert f"#define APSP_TILE {apsp.TILE}" in text
     assert f"#define APSP_MAX_N {apsp.MAX_N}" in text
+    assert "APSP_ENEGCYCLE = 6" in text and apsp.ENEGCYCLE == 6
+    sparse = open(os.path.join(ROOT, "include", "apsp_sparse.h")).read()
+    assert f"#define APSP_SPARSE_MAX_N {apsp.SPARSE_MAX_N}" in sparse
 
 
 def test_status_strings_and_version(libs):
     lib = apsp.load()
-    for code in range(6):
+    for code in range(7):
         s = lib.apsp_status_string(code).decode()
         assert s.startswith("APSP_")
     assert lib.apsp_status_string(99).decode() == "unknown apsp status"
@@ -67,6 +71,29 @@ def test_bad_arguments_rejected_without_cuda(libs):
     assert lib.apsp_phase_timing_enable(0) == apsp.OK
     assert lib.apsp_debug_inject_phase3_timeout(0) == apsp.EINVAL
     assert lib.apsp_debug_inject_phase3_timeout(3 * 10**9) == apsp.EINVAL
+
+
+def test_sparse_bad_arguments_rejected_without_cuda(libs):
+    lib = apsp.load()
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    big = apsp.SPARSE_MAX_N + 1
+    assert lib.apsp_solve_sparse_i32(None, 5, 5, 0, None) == apsp.EINVAL
+    assert lib.apsp_solve_sparse_i32(fake, 6, 5, 0, None) == apsp.EINVAL
+    assert lib.apsp_solve_sparse_i32(fake, big, big, 0, None) == apsp.EINVAL
+    assert lib.apsp_solve_sparse_i32(None, 0, 0, 0, None) == apsp.OK
+    assert lib.apsp_johnson_csr_i32(None, fake, fake, 5, 0, fake, 5, None) == apsp.EINVAL
+    assert lib.apsp_johnson_csr_i32(fake, fake, fake, 5, 0, None, 5, None) == apsp.EINVAL
+    assert lib.apsp_johnson_csr_i32(fake, fake, fake, 5, 0, fake, 4, None) == apsp.EINVAL
+    assert lib.apsp_johnson_csr_i32(None, None, None, 0, 0, None, 0, None) == apsp.OK
+    assert lib.apsp_sssp_delta_i32(fake, fake, fake, 5, fake, 2, 0, fake, 4, None) == apsp.EINVAL
+    assert lib.apsp_sssp_delta_i32(fake, fake, fake, 5, None, 2, 0, fake, 5, None) == apsp.EINVAL
+    assert lib.apsp_sssp_delta_i32(fake, fake, fake, 5, fake, -1, 0, fake, 5, None) == apsp.EINVAL
+    assert lib.apsp_sssp_delta_i32(fake, fake, fake, 5, fake, 0, 0, fake, 5, None) == apsp.OK
+    m = ctypes.c_longlong(0)
+    assert lib.apsp_csr_count_i32(fake, 4, 4, None, ctypes.byref(m), None) == apsp.EINVAL
+    assert lib.apsp_csr_count_i32(fake, 4, 3, fake, ctypes.byref(m), None) == apsp.EINVAL
+    assert lib.apsp_csr_fill_i32(fake, 4, 4, fake, None, fake, None) == apsp.EINVAL
+    assert lib.apsp_csr_fill_i32(None, 0, 0, None, None, None, None) == apsp.OK
 
 
 def test_python_binding_rejects_non_cuda():
