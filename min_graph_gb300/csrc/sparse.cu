@@ -47,8 +47,6 @@ namespace {
 
 constexpr int32_t kInf = APSP_INF_I32;
 constexpr int32_t kUnreached = INT_MAX;
-constexpr int kSpThreads = 512;
-constexpr int kSpWarps = kSpThreads / 32;
 constexpr int kScanThreads = 1024;
 
 apsp_status_t sp_fail(cudaError_t e) {
@@ -205,67 +203,182 @@ __global__ void reweight_kernel(const int64_t* __restrict__ rp, const int32_t* _
 
 // ------------------------------------------------------------------ Delta-stepping
 
+// Light-first partition of each vertex's arcs against delta, packed as
+// (head, weight) pairs: arcs[rp[u] .. rp[u] + nlight[u]) are the light arcs
+// (w <= delta) of u and the rest of its range the heavy ones, each part in
+// CSR order (warp per vertex, two ballot passes).
+__global__ void partition_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                                 const int32_t* __restrict__ w, int n, int32_t delta, int2* __restrict__ arcs,
+                                 int32_t* __restrict__ nlight) {
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= n) return;
+    const int u = (int)wid;
+    const int64_t beg = rp[u], end = rp[u + 1];
+    int nl = 0;
+    for (int64_t e = beg + lane; e < end; e += 32) nl += w[e] <= delta ? 1 : 0;
+    nl = __reduce_add_sync(0xffffffffu, nl);
+    const unsigned lt = (1u << lane) - 1u;
+    int64_t lpos = beg, hpos = beg + nl;
+    for (int64_t e0 = beg; e0 < end; e0 += 32) {
+        const int64_t e = e0 + lane;
+        const bool valid = e < end;
+        const int32_t c = valid ? col[e] : 0, ww = valid ? w[e] : 0;
+        const bool light = valid && ww <= delta, heavy = valid && ww > delta;
+        const unsigned ml = __ballot_sync(0xffffffffu, light), mh = __ballot_sync(0xffffffffu, heavy);
+        if (light) arcs[lpos + __popc(ml & lt)] = make_int2(c, ww);
+        if (heavy) arcs[hpos + __popc(mh & lt)] = make_int2(c, ww);
+        lpos += __popc(ml);
+        hpos += __popc(mh);
+    }
+    if (lane == 0) nlight[u] = nl;
+}
+
 struct SpShared {
-    int qlen;
-    int bmin;
+    int dmin[2];  // least queued distance, double-buffered by bucket parity
     int item;
 };
 
+// Shared memory of a search CTA: dist (int32, n) and the queued bitmap.
 __host__ __device__ constexpr size_t sssp_shared_offset(int n) {
-    return ((size_t)n * 4 + (size_t)((n + 31) / 32) * 8 + (size_t)n * 2 + 15) / 16 * 16;
+    return ((size_t)n * 4 + (size_t)((n + 31) / 32) * 4 + 15) / 16 * 16;
 }
 
 size_t sssp_smem_bytes(int n) { return sssp_shared_offset(n) + sizeof(SpShared); }
 
-// Relax the arcs of frontier vertices queue[0..qlen) whose weight is light
-// (kLight) or heavy (!kLight) against delta.
-template <bool kLight>
-__device__ __forceinline__ void relax_frontier(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
-                                               const int32_t* __restrict__ w, int32_t delta,
-                                               const uint16_t* queue, int qlen, int32_t* dist,
-                                               uint32_t* queued, int warp, int lane) {
-    for (int qi = warp; qi < qlen; qi += kSpWarps) {
-        const int v = queue[qi];
-        const uint32_t dv = (uint32_t)dist[v];
-        const int64_t e1 = rp[v + 1];
-        for (int64_t e = rp[v] + lane; e < e1; e += 32) {
-            const int32_t we = w[e];
-            if (kLight ? we > delta : we <= delta) continue;
-            const uint32_t s = dv + (uint32_t)we;  // < 2^32: both terms < 2^31
-            const int32_t nd = s >= (uint32_t)kUnreached ? kUnreached : (int32_t)s;
-            const int u = col[e];
-            if (nd < dist[u] && nd < atomicMin(dist + u, nd)) atomicOr(queued + (u >> 5), 1u << (u & 31));
+// Position of the k-th (0-based) set bit of x; x has more than k set bits.
+__device__ __forceinline__ int kth_set_bit(uint32_t x, int k) {
+    int pos = 0;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) {
+        const int c = __popc(x & ((1u << s) - 1u));
+        if (k >= c) {
+            k -= c;
+            x >>= s;
+            pos += s;
         }
     }
+    return pos;
 }
 
-// Append the members of `sel` (word i of a bitmap) to the frontier list.
-__device__ __forceinline__ void push_bits(uint32_t sel, int i, uint16_t* queue, int* qlen) {
-    int p = atomicAdd(qlen, __popc(sel));
-    while (sel) {
-        const int b = __ffs(sel) - 1;
-        sel &= sel - 1;
-        queue[p++] = (uint16_t)(i * 32 + b);
+// Largest lane j with key_j <= t, for keys non-decreasing across the warp
+// and key_0 <= t.
+__device__ __forceinline__ int last_lane_at_or_below(int key, int t) {
+    int pos = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+        const int x = __shfl_sync(0xffffffffu, key, pos + step);
+        if (x <= t) pos += step;
     }
+    return pos;
+}
+
+// Relax the light (kLight) or heavy arcs of the warp's frontier.  Lane j
+// holds in `bits` the frontier members of bitmap word j * kWarps + warp.
+// A warp scan numbers the members 0 .. T-1 and they are taken 32 at a time,
+// so every batch but the last is full: lane k finds the word and the bit of
+// member b + k, loads that vertex's arc range, a second warp scan lays the
+// 32 ranges end to end, and the lanes walk the concatenation in chunks of 32
+// arcs, up to kUnroll chunks with their loads in flight together.  Returns
+// this lane's least distance among its successful relaxations (INT_MAX if
+// none).
+template <bool kLight, int kWarps, int kUnroll>
+__device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restrict__ rp,
+                                          const int32_t* __restrict__ nlight, const int2* __restrict__ arcs,
+                                          int32_t* dist, uint32_t* queued, int warp, int lane) {
+    int32_t best = INT_MAX;
+    const int c = __popc(bits);
+    int wincl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += y;
+    }
+    const int members = __shfl_sync(0xffffffffu, wincl, 31);
+    const int wexcl = wincl - c;
+    for (int b0 = 0; b0 < members; b0 += 32) {
+        const int g = b0 + lane;
+        const int j = last_lane_at_or_below(wexcl, g);
+        const uint32_t wbits = __shfl_sync(0xffffffffu, bits, j);
+        const int wstart = __shfl_sync(0xffffffffu, wexcl, j);
+        int beg = 0, cnt = 0;
+        uint32_t dv = 0;
+        if (g < members) {
+            const int v = (j * kWarps + warp) * 32 + kth_set_bit(wbits, g - wstart);
+            const int r0 = (int)rp[v], nl = nlight[v];
+            if (kLight) {
+                beg = r0;
+                cnt = nl;
+            } else {
+                beg = r0 + nl;
+                cnt = (int)rp[v + 1] - r0 - nl;
+            }
+            dv = (uint32_t)dist[v];
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        const int excl = incl - cnt;
+        for (int base = 0; base < total; base += 32 * kUnroll) {
+            int2 a[kUnroll];
+            uint32_t d[kUnroll];
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                const int t = base + q * 32 + lane;
+                const int pos = last_lane_at_or_below(excl, t);
+                const int e = __shfl_sync(0xffffffffu, beg, pos) + t - __shfl_sync(0xffffffffu, excl, pos);
+                d[q] = __shfl_sync(0xffffffffu, dv, pos);
+                a[q] = t < total ? arcs[e] : make_int2(0, -1);
+            }
+#pragma unroll
+            for (int q = 0; q < kUnroll; ++q) {
+                if (a[q].y < 0) continue;  // past the end (weights here are >= 0)
+                const uint32_t s = d[q] + (uint32_t)a[q].y;  // < 2^32: both terms < 2^31
+                const int32_t nd = s >= (uint32_t)kUnreached ? kUnreached : (int32_t)s;
+                const int u = a[q].x;
+                if (nd < dist[u] && nd < atomicMin(dist + u, nd)) {
+                    atomicOr(queued + (u >> 5), 1u << (u & 31));
+                    best = min(best, nd);
+                }
+            }
+        }
+    }
+    return best;
 }
 
 // Row `item` of out gets the distances from source sources[item] (or item
 // when sources is null).  With h non-null the search ran on reweighted arcs
 // and the epilogue maps back: out = dist + h[v] - h[src].  A source outside
 // [0, n) sets bit 0 of *err and its row is skipped.
-__global__ void __launch_bounds__(kSpThreads, 1)
-sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
-                  const int32_t* __restrict__ w, int n, const int32_t* __restrict__ sources, int nsrc,
+//
+// Lane j of warp w owns bitmap word j * kWarps + w (n <= 1024 * kWarps):
+// it selects that word's queued vertices into its frontier register F and
+// accumulates R (removed from the current bucket) in another register.
+// Per bucket: light phases (select the queued vertices below the bucket's
+// upper end hi, relax their light arcs) until a selection comes back empty;
+// that last selection also yields the least queued distance at or above hi.
+// Then the heavy arcs of R; their successful relaxations, with that least
+// distance, give the next bucket.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, 1536 / kThreads)
+sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nlight,
+                  const int2* __restrict__ arcs, int n, const int32_t* __restrict__ sources, int nsrc,
                   int32_t delta, const long long* __restrict__ h, int32_t* __restrict__ out, long long ldo,
                   int* __restrict__ counter, int* __restrict__ err) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kUnroll = 2;
     extern __shared__ __align__(16) unsigned char sp_smem[];
     const int nw = (n + 31) / 32;
     int32_t* dist = reinterpret_cast<int32_t*>(sp_smem);
-    uint32_t* queued = reinterpret_cast<uint32_t*>(dist + n);
-    uint32_t* rset = queued + nw;
-    uint16_t* queue = reinterpret_cast<uint16_t*>(rset + nw);
+    uint32_t* queued = reinterpret_cast<uint32_t*>(dist + n);  // waiting in some bucket
     SpShared* sh = reinterpret_cast<SpShared*>(sp_smem + sssp_shared_offset(n));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int myword = lane * kWarps + warp;
+    const bool owns = myword < nw;
 
     for (;;) {
         if (tid == 0) sh->item = atomicAdd(counter, 1);
@@ -278,10 +391,11 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ co
             if (tid == 0) atomicOr(err, 1);
             continue;
         }
-        for (int v = tid; v < n; v += kSpThreads) dist[v] = kUnreached;
-        for (int i = tid; i < nw; i += kSpThreads) {
-            queued[i] = 0u;
-            rset[i] = 0u;
+        for (int v = tid; v < n; v += kThreads) dist[v] = kUnreached;
+        for (int i = tid; i < nw; i += kThreads) queued[i] = 0u;
+        if (tid == 0) {
+            sh->dmin[0] = INT_MAX;
+            sh->dmin[1] = INT_MAX;
         }
         __syncthreads();
         if (tid == 0) {
@@ -290,67 +404,48 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ co
         }
         __syncthreads();
 
-        for (;;) {
-            // the lowest non-empty bucket
-            if (tid == 0) sh->bmin = INT_MAX;
-            __syncthreads();
-            int local = INT_MAX;
-            for (int i = tid; i < nw; i += kSpThreads) {
-                uint32_t bits = queued[i];
-                while (bits) {
-                    const int b = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    local = min(local, dist[i * 32 + b] / delta);
-                }
-            }
-            local = __reduce_min_sync(0xffffffffu, local);
-            if (lane == 0 && local != INT_MAX) atomicMin(&sh->bmin, local);
-            __syncthreads();
-            const int bmin = sh->bmin;
-            if (bmin == INT_MAX) break;
-
-            // light phases until the bucket stays empty
+        int32_t dmin = 0;  // least queued distance: the current bucket is [.., hi)
+        for (int bucket = 0;; ++bucket) {
+            const long long hi_ll = ((long long)(dmin / delta) + 1) * delta;
+            const int32_t hi = hi_ll >= kUnreached ? kUnreached : (int32_t)hi_ll;
+            uint32_t rbits = 0u;  // R, this lane's word
+            int32_t beyond;       // least queued distance >= hi seen by the last selection
             for (;;) {
-                if (tid == 0) sh->qlen = 0;
-                __syncthreads();
-                for (int i = tid; i < nw; i += kSpThreads) {
-                    uint32_t bits = queued[i], sel = 0u;
+                beyond = INT_MAX;
+                uint32_t fbits = 0u;
+                if (owns) {
+                    uint32_t bits = queued[myword];
+                    const uint32_t all = bits;
                     while (bits) {
                         const int b = __ffs(bits) - 1;
                         bits &= bits - 1;
-                        if (dist[i * 32 + b] / delta == bmin) sel |= 1u << b;
+                        const int32_t dd = dist[myword * 32 + b];
+                        if (dd < hi)
+                            fbits |= 1u << b;
+                        else
+                            beyond = min(beyond, dd);
                     }
-                    if (sel) {
-                        queued[i] &= ~sel;
-                        rset[i] |= sel;
-                        push_bits(sel, i, queue, &sh->qlen);
-                    }
+                    if (fbits) queued[myword] = all & ~fbits;
+                    rbits |= fbits;
                 }
-                __syncthreads();
-                const int qlen = sh->qlen;
-                if (qlen == 0) break;
-                relax_frontier<true>(rp, col, w, delta, queue, qlen, dist, queued, warp, lane);
+                if (!__syncthreads_or(fbits != 0u)) break;
+                expand<true, kWarps, kUnroll>(fbits, rp, nlight, arcs, dist, queued, warp, lane);
                 __syncthreads();
             }
-
-            // heavy arcs of R, once
-            if (tid == 0) sh->qlen = 0;
+            // heavy arcs of R, once; then the next bucket from the least queued distance
+            const int32_t hbest = expand<false, kWarps, kUnroll>(rbits, rp, nlight, arcs, dist, queued, warp, lane);
+            const int32_t next = __reduce_min_sync(0xffffffffu, min(beyond, hbest));
+            const int slot = bucket & 1;
+            if (lane == 0 && next != INT_MAX) atomicMin(&sh->dmin[slot], next);
             __syncthreads();
-            for (int i = tid; i < nw; i += kSpThreads) {
-                const uint32_t sel = rset[i];
-                if (sel) {
-                    rset[i] = 0u;
-                    push_bits(sel, i, queue, &sh->qlen);
-                }
-            }
-            __syncthreads();
-            relax_frontier<false>(rp, col, w, delta, queue, sh->qlen, dist, queued, warp, lane);
-            __syncthreads();
+            dmin = sh->dmin[slot];
+            if (dmin == INT_MAX) break;
+            if (tid == 0) sh->dmin[slot ^ 1] = INT_MAX;  // last read a bucket ago; next written after a barrier
         }
 
         int32_t* orow = out + (long long)item * ldo;
         const long long hs = h ? h[src] : 0;
-        for (int v = tid; v < n; v += kSpThreads) {
+        for (int v = tid; v < n; v += kThreads) {
             const int32_t dv = dist[v];
             long long r = dv;
             if (h && dv != kUnreached) r = (long long)dv + h[v] - hs;
@@ -404,7 +499,8 @@ SparseState* sp_state() {
 
 int blocks_for_warps(long long warps) { return (int)((warps * 32 + 255) / 256); }
 
-// work buffer: [0, 256) small counters, then h (int64 n), then w' (int32 m)
+// Work buffer: [0, 256) small counters, then h (int64, n), w' (int32, m),
+// the partitioned arcs (int2, m) and the light-arc counts (int32, n).
 struct Work {
     int* range;    // [0] min, [1] max, [2] bad head
     int* counter;  // source counter of the search
@@ -412,21 +508,31 @@ struct Work {
     int* err;      // search error bits
     long long* h;
     int32_t* wh;
+    int2* arcs;
+    int32_t* nlight;
 };
 
 size_t work_bytes(int n, long long m) {
-    return 256 + align256((size_t)n * 8) + align256((size_t)(m > 0 ? m : 1) * 4);
+    const size_t mm = (size_t)(m > 0 ? m : 1);
+    return 256 + align256((size_t)n * 8) + align256(mm * 4) + align256(mm * 8) + align256((size_t)n * 4);
 }
 
-Work work_layout(void* base, int n) {
+Work work_layout(void* base, int n, long long m) {
+    const size_t mm = (size_t)(m > 0 ? m : 1);
     char* b = static_cast<char*>(base);
     Work wk;
     wk.range = reinterpret_cast<int*>(b);
     wk.counter = wk.range + 4;
     wk.changed = wk.range + 5;
     wk.err = wk.range + 6;
-    wk.h = reinterpret_cast<long long*>(b + 256);
-    wk.wh = reinterpret_cast<int32_t*>(b + 256 + align256((size_t)n * 8));
+    size_t off = 256;
+    wk.h = reinterpret_cast<long long*>(b + off);
+    off += align256((size_t)n * 8);
+    wk.wh = reinterpret_cast<int32_t*>(b + off);
+    off += align256(mm * 4);
+    wk.arcs = reinterpret_cast<int2*>(b + off);
+    off += align256(mm * 8);
+    wk.nlight = reinterpret_cast<int32_t*>(b + off);
     return wk;
 }
 
@@ -482,42 +588,66 @@ apsp_status_t check_row_ptr(const int64_t* rp, int n, int* flag, cudaStream_t s)
     return bad ? APSP_EINVAL : APSP_OK;
 }
 
-// Bucket width when the caller gives none: the largest arc weight spread
-// over a few out-degrees, so that a bucket holds several hops of the
-// search front.
+// Bucket width when the caller gives none: 3 * w_max / (mean out-degree),
+// so that with weights spread over [0, w_max] a vertex has about three light
+// arcs.  The Delta-stepping page tunes Delta by measurement (section 4.4);
+// the factor 3 was the fastest here on the Erdos-Renyi and Barabasi-Albert
+// workloads.
 int32_t default_delta(int n, long long m, int wmax) {
     if (m <= 0 || wmax <= 0) return 1;
     const double avg_deg = (double)m / (double)(n > 0 ? n : 1);
-    double d = 8.0 * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
+    double d = 3.0 * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
     if (d < 1.0) d = 1.0;
     if (d > (double)kInf) d = (double)kInf;
     return (int32_t)d;
 }
 
-apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, const int32_t* sources,
-                          int nsrc, int32_t delta, const long long* h, int32_t* out, long long ldo, const Work& wk,
-                          cudaStream_t s) {
+template <int kThreads>
+apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int32_t* sources, int nsrc,
+                            int32_t delta, const long long* h, int32_t* out, long long ldo, size_t smem, int grid,
+                            cudaStream_t s) {
+    sssp_delta_kernel<kThreads><<<grid, kThreads, smem, s>>>(rp, wk.nlight, wk.arcs, n, sources, nsrc, delta, h,
+                                                             out, ldo, wk.counter, wk.err);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? APSP_OK : sp_fail(e);
+}
+
+// Partition the arcs against delta, then one persistent search CTA per
+// resident slot.  512 threads a CTA while at least two CTAs fit an SM (n up
+// to about 24K), else 1024 threads in one CTA.
+apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m,
+                          const int32_t* sources, int nsrc, int32_t delta, const long long* h, int32_t* out,
+                          long long ldo, const Work& wk, cudaStream_t s) {
+    partition_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, delta, wk.arcs, wk.nlight);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    (void)m;
     const size_t smem = sssp_smem_bytes(n);
-    cudaError_t e = cudaFuncSetAttribute(sssp_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(sssp_delta_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sssp_delta_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return sp_fail(e);
     int dev = 0, sms = 0, per_sm = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel, kSpThreads, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel<512>, 512, smem);
     if (e != cudaSuccess) return sp_fail(e);
+    const bool wide = n > 1024 * (512 / 32) || per_sm < 2;  // the 512-thread CTA covers n <= 16384
+    if (wide) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel<1024>, 1024, smem);
+        if (e != cudaSuccess) return sp_fail(e);
+    }
     if (per_sm < 1) return APSP_EUNSUPPORTED;
     long long grid = (long long)sms * per_sm;
     if (grid > nsrc) grid = nsrc;
     e = cudaMemsetAsync(wk.counter, 0, sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(wk.err, 0, sizeof(int), s);
     if (e != cudaSuccess) return sp_fail(e);
-    sssp_delta_kernel<<<(unsigned)grid, kSpThreads, smem, s>>>(rp, col, w, n, sources, nsrc, delta, h, out, ldo,
-                                                               wk.counter, wk.err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return sp_fail(e);
+    apsp_status_t rc = wide ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
+                            : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
+    if (rc != APSP_OK) return rc;
     int err = 0;
-    apsp_status_t rc = read_int(wk.err, &err, s);
+    rc = read_int(wk.err, &err, s);
     if (rc != APSP_OK) return rc;
     return err ? APSP_EINVAL : APSP_OK;
 }
@@ -567,7 +697,7 @@ apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, i
         if (rc != APSP_OK) return rc;
     }
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(rp, col, wuse, n, nullptr, n, delta, huse, out, ld, wk, s);
+    return launch_sssp(rp, col, wuse, n, m, nullptr, n, delta, huse, out, ld, wk, s);
 }
 
 // CSR of a dense matrix into st.rp / st.body; returns m.
@@ -645,9 +775,10 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
     apsp_status_t rc = read_m(row_ptr, n, &m, s);
     if (rc != APSP_OK) return rc;
     if (m < 0 || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
-    rc = grow(st->work, 256);
+    if (m >= (long long)INT_MAX) return APSP_EINVAL;  // arc indices are int32 in the search
+    rc = grow(st->work, work_bytes(n, m));
     if (rc != APSP_OK) return rc;
-    const Work wk = work_layout(st->work.p, 0);
+    const Work wk = work_layout(st->work.p, n, m);
     rc = check_row_ptr(row_ptr, n, wk.err, s);
     if (rc != APSP_OK) return rc;
     int lo = 0, hi = 0, bad = 0;
@@ -655,7 +786,7 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
     if (rc != APSP_OK) return rc;
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(row_ptr, col_idx, w, n, sources, nsrc, delta, nullptr, out, ldo, wk, s);
+    return launch_sssp(row_ptr, col_idx, w, n, m, sources, nsrc, delta, nullptr, out, ldo, wk, s);
 }
 
 apsp_status_t apsp_johnson_csr_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
@@ -672,9 +803,10 @@ apsp_status_t apsp_johnson_csr_i32(const int64_t* row_ptr, const int32_t* col_id
     apsp_status_t rc = read_m(row_ptr, n, &m, s);
     if (rc != APSP_OK) return rc;
     if (m < 0 || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
+    if (m >= (long long)INT_MAX) return APSP_EINVAL;  // arc indices are int32 in the search
     rc = grow(st->work, work_bytes(n, m));
     if (rc != APSP_OK) return rc;
-    const Work wk = work_layout(st->work.p, n);
+    const Work wk = work_layout(st->work.p, n, m);
     rc = check_row_ptr(row_ptr, n, wk.err, s);
     if (rc != APSP_OK) return rc;
     return johnson(row_ptr, col_idx, w, n, m, delta, out, ld, wk, true, s);
@@ -698,7 +830,7 @@ apsp_status_t apsp_solve_sparse_i32(int32_t* dist, int n, int ld, int32_t delta,
     const int32_t* col = static_cast<const int32_t*>(st->body.p);
     const int32_t* w = reinterpret_cast<const int32_t*>(static_cast<const char*>(st->body.p) + colb);
     // The searches read only the CSR, so they may overwrite dist as they go.
-    return johnson(rp, col, w, n, m, delta, dist, ld, work_layout(st->work.p, n), false, s);
+    return johnson(rp, col, w, n, m, delta, dist, ld, work_layout(st->work.p, n, m), false, s);
 }
 
 apsp_status_t apsp_sparse_release(void) {
