@@ -61,6 +61,20 @@ int apsp_peak_addmin(int variant, int blocks, int threads, int iters, double* re
 /* Number of variants understood by apsp_peak_addmin. */
 int apsp_peak_variants(void);
 
+/*
+ * apsp_peak_l2_read -- read bandwidth of the L2 cache: a buffer of `bytes`
+ * (16 B .. 256 MiB; choose it well inside the L2) is read once to bring it
+ * into L2, then `passes` more times with 16-byte loads that bypass L1, by
+ * `blocks` x `threads` threads in a grid-stride loop.  This is the
+ * denominator of the sparse searches' roofline, whose arc stream is served
+ * from L2.
+ *   gbs  bytes read per second / 1e9 over the timed passes (CUDA events).
+ *   ms   time of the timed passes.
+ * Returns 0, -1 on a bad argument, or a cudaError_t value (> 0).
+ * Allocates and frees its buffer; synchronises the device.
+ */
+int apsp_peak_l2_read(long long bytes, int blocks, int threads, int passes, double* gbs, double* ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -46,13 +46,14 @@
  * return.  They read the arc count, and Bellman-Ford's round flags, on the
  * host.  Kernel faults therefore show up in the return value.
  *
- * Workspace: a per-device buffer, grown on demand and freed by
- * apsp_sparse_release().  It holds the CSR built from a dense matrix, h and
- * w'.  The caller owns every pointer passed in.
+ * Workspace: per-device buffers, grown on demand and freed by
+ * apsp_sparse_release().  They hold the CSR built from a dense matrix, h,
+ * w', and the arcs partitioned light-first against Delta.  The caller owns
+ * every pointer passed in.
  *
- * Limits: n <= APSP_SPARSE_MAX_N.  Each CTA keeps one source's distances,
- * two vertex bitmaps and a vertex queue in shared memory, 6.25 bytes per
- * vertex.
+ * Limits: n <= APSP_SPARSE_MAX_N.  Each search CTA keeps one source's
+ * distances and a bitmap of queued vertices in shared memory, 4.125 bytes
+ * per vertex.
  *
  * Thread safety: any host thread may call these.  Sparse calls on one
  * process are serialised by a lock.
@@ -124,6 +125,17 @@ apsp_status_t apsp_csr_fill_i32(const int32_t* dist, int n, int ld, const int64_
 
 /* Free the sparse workspace on every device that has one. */
 apsp_status_t apsp_sparse_release(void);
+
+/*
+ * apsp_sparse_timing_enable / _read -- measurement hooks for the bench.
+ * While enabled, each search launch is bracketed by CUDA events on its
+ * stream.  _read returns, and resets, the summed search-kernel time in ms,
+ * the number of search launches, and the number of kernels the sparse entry
+ * points launched (counted whether or not timing is enabled).  Any pointer
+ * may be NULL.
+ */
+apsp_status_t apsp_sparse_timing_enable(int enable);
+apsp_status_t apsp_sparse_timing_read(double* search_ms, long long* searches, long long* kernels);
 
 #ifdef __cplusplus
 }

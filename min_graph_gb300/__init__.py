@@ -100,6 +100,11 @@ def load():
         lib.apsp_csr_fill_i32.restype = i32
         lib.apsp_sparse_release.argtypes = []
         lib.apsp_sparse_release.restype = i32
+        lib.apsp_sparse_timing_enable.argtypes = [i32]
+        lib.apsp_sparse_timing_enable.restype = i32
+        lib.apsp_sparse_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
+                                                ctypes.POINTER(i64)]
+        lib.apsp_sparse_timing_read.restype = i32
         _lib = lib
         return lib
 
@@ -352,3 +357,16 @@ def sssp_delta(row_ptr, col_idx, w, sources, delta: int = 0, out=None, stream=No
 
 def sparse_release() -> None:
     _check(load().apsp_sparse_release(), "apsp_sparse_release")
+
+
+def sparse_timing_enable(enable: bool = True) -> None:
+    _check(load().apsp_sparse_timing_enable(int(bool(enable))), "apsp_sparse_timing_enable")
+
+
+def sparse_timing_read():
+    """(search-kernel ms, search launches, sparse kernel launches) since the
+    last read (include/apsp_sparse.h)."""
+    ms, n, k = ctypes.c_double(), ctypes.c_longlong(), ctypes.c_longlong()
+    _check(load().apsp_sparse_timing_read(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(k)),
+           "apsp_sparse_timing_read")
+    return ms.value, n.value, k.value

@@ -268,6 +268,52 @@ int run(int blocks, int threads, int iters, double* rpc, double* ms_out, long lo
 
 }  // namespace
 
+// L2 read probe: grid-stride 16-byte loads over a buffer small enough to
+// stay in L2, `passes` times; the XOR of what was read is stored once per
+// thread so the loads cannot be dropped.
+__global__ void l2_read_kernel(const int4* __restrict__ buf, long long n16, int passes, int* __restrict__ sink) {
+    int acc = 0;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (int p = 0; p < passes; ++p) {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+            const int4 v = __ldcg(buf + i);
+            acc ^= v.x ^ v.y ^ v.z ^ v.w;
+        }
+    }
+    sink[(long long)blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+
+extern "C" int apsp_peak_l2_read(long long bytes, int blocks, int threads, int passes, double* gbs, double* ms) {
+    if (bytes < 16 || bytes > (256ll << 20) || blocks <= 0 || threads <= 0 || threads > 1024 || passes <= 0)
+        return -1;
+    const long long n16 = bytes / 16;
+    int4* buf = nullptr;
+    int* sink = nullptr;
+    cudaError_t e = cudaMalloc(&buf, n16 * 16);
+    if (e == cudaSuccess) e = cudaMalloc(&sink, (size_t)blocks * threads * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(buf, 1, n16 * 16);
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (e == cudaSuccess) e = cudaEventCreate(&a);
+    if (e == cudaSuccess) e = cudaEventCreate(&b);
+    float t = 0.f;
+    if (e == cudaSuccess) {
+        l2_read_kernel<<<blocks, threads>>>(buf, n16, 1, sink);  // warm: brings the buffer into L2
+        cudaEventRecord(a);
+        l2_read_kernel<<<blocks, threads>>>(buf, n16, passes, sink);
+        cudaEventRecord(b);
+        e = cudaEventSynchronize(b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, a, b);
+    }
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+    cudaFree(buf);
+    cudaFree(sink);
+    if (e != cudaSuccess) return (int)e;
+    if (ms) *ms = t;
+    if (gbs) *gbs = (double)n16 * 16 * passes / (t * 1e-3) / 1e9;
+    return 0;
+}
+
 extern "C" int apsp_peak_variants(void) { return 21; }
 
 extern "C" int apsp_peak_addmin(int variant, int blocks, int threads, int iters, double* rpc,

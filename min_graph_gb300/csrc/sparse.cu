@@ -469,6 +469,19 @@ struct SparseState {
 std::mutex g_sp_mu;
 std::vector<SparseState> g_sp;
 
+// Optional timing of the search kernel (apsp_sparse_timing_*), under g_sp_mu.
+struct SparseTiming {
+    bool enabled = false;
+    double search_ms = 0.0;
+    long long searches = 0;
+    long long kernels = 0;  // every kernel launched by the sparse entry points
+};
+SparseTiming g_sp_timing;
+
+// Kernel launches of the sparse entry points are counted for the timing API
+// (callers hold g_sp_mu).
+inline void count_kernel(int k = 1) { g_sp_timing.kernels += k; }
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 apsp_status_t grow(DevBuf& b, size_t need) {
@@ -561,6 +574,7 @@ apsp_status_t weight_range(const int32_t* w, const int32_t* col, long long m, in
         long long blocks = (m + 255) / 256;
         if (blocks > 4096) blocks = 4096;
         weight_range_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, col, m, n, range);
+        count_kernel();
         e = cudaGetLastError();
         if (e != cudaSuccess) return sp_fail(e);
     }
@@ -580,6 +594,7 @@ apsp_status_t check_row_ptr(const int64_t* rp, int n, int* flag, cudaStream_t s)
     cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
     if (e != cudaSuccess) return sp_fail(e);
     rowptr_check_kernel<<<(n + 1 + 255) / 256, 256, 0, s>>>(rp, n, flag);
+    count_kernel();
     e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     int bad = 0;
@@ -643,11 +658,38 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
     e = cudaMemsetAsync(wk.counter, 0, sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(wk.err, 0, sizeof(int), s);
     if (e != cudaSuccess) return sp_fail(e);
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    if (g_sp_timing.enabled) {
+        e = cudaEventCreate(&ev[0]);
+        if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[0], s);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t x : ev)
+                if (x) cudaEventDestroy(x);
+            return sp_fail(e);
+        }
+    }
     apsp_status_t rc = wide ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
                             : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
-    if (rc != APSP_OK) return rc;
+    count_kernel(2);  // partition + search
+    if (rc == APSP_OK && ev[1]) {
+        e = cudaEventRecord(ev[1], s);
+        if (e != cudaSuccess) rc = sp_fail(e);
+    }
     int err = 0;
-    rc = read_int(wk.err, &err, s);
+    if (rc == APSP_OK) rc = read_int(wk.err, &err, s);  // waits for the search
+    if (rc == APSP_OK && ev[1]) {
+        float t = 0.f;
+        e = cudaEventElapsedTime(&t, ev[0], ev[1]);
+        if (e != cudaSuccess) {
+            rc = sp_fail(e);
+        } else {
+            g_sp_timing.search_ms += t;
+            g_sp_timing.searches += 1;
+        }
+    }
+    for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
     if (rc != APSP_OK) return rc;
     return err ? APSP_EINVAL : APSP_OK;
 }
@@ -671,6 +713,7 @@ apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, i
             e = cudaMemsetAsync(wk.changed, 0, sizeof(int), s);
             if (e != cudaSuccess) return sp_fail(e);
             bf_round_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, wk.h, wk.changed);
+            count_kernel();
             e = cudaGetLastError();
             if (e != cudaSuccess) return sp_fail(e);
             int changed = 0;
@@ -685,6 +728,7 @@ apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, i
         e = cudaMemsetAsync(wk.changed, 0, sizeof(int), s);
         if (e != cudaSuccess) return sp_fail(e);
         reweight_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, wk.h, wk.wh, wk.changed);
+        count_kernel();
         e = cudaGetLastError();
         if (e != cudaSuccess) return sp_fail(e);
         int range_bad = 0;
@@ -707,6 +751,7 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
     int64_t* rp = static_cast<int64_t*>(st.rp.p);
     csr_count_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, rp);
     scan_kernel<<<1, kScanThreads, 0, s>>>(rp, n);
+    count_kernel(2);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     long long m = 0;
@@ -718,6 +763,7 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
     int32_t* col = static_cast<int32_t*>(st.body.p);
     int32_t* w = reinterpret_cast<int32_t*>(static_cast<char*>(st.body.p) + colb);
     csr_fill_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, rp, col, w);
+    count_kernel();
     e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     *m_out = m;
@@ -742,6 +788,10 @@ apsp_status_t apsp_csr_count_i32(const int32_t* dist, int n, int ld, int64_t* ro
     }
     csr_count_kernel<<<blocks_for_warps(n), 256, 0, s>>>(dist, ld, n, row_ptr);
     scan_kernel<<<1, kScanThreads, 0, s>>>(row_ptr, n);
+    {
+        std::lock_guard<std::mutex> lock(g_sp_mu);
+        count_kernel(2);
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     return read_m(row_ptr, n, m_out, s);
@@ -755,6 +805,10 @@ apsp_status_t apsp_csr_fill_i32(const int32_t* dist, int n, int ld, const int64_
     if (n == 0) return APSP_OK;
     if (!sp_supported_device()) return APSP_EUNSUPPORTED;
     csr_fill_kernel<<<blocks_for_warps(n), 256, 0, (cudaStream_t)stream>>>(dist, ld, n, row_ptr, col_idx, w);
+    {
+        std::lock_guard<std::mutex> lock(g_sp_mu);
+        count_kernel();
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     return APSP_OK;
@@ -831,6 +885,23 @@ apsp_status_t apsp_solve_sparse_i32(int32_t* dist, int n, int ld, int32_t delta,
     const int32_t* w = reinterpret_cast<const int32_t*>(static_cast<const char*>(st->body.p) + colb);
     // The searches read only the CSR, so they may overwrite dist as they go.
     return johnson(rp, col, w, n, m, delta, dist, ld, work_layout(st->work.p, n, m), false, s);
+}
+
+apsp_status_t apsp_sparse_timing_enable(int enable) {
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    g_sp_timing.enabled = enable != 0;
+    return APSP_OK;
+}
+
+apsp_status_t apsp_sparse_timing_read(double* search_ms, long long* searches, long long* kernels) {
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    if (search_ms) *search_ms = g_sp_timing.search_ms;
+    if (searches) *searches = g_sp_timing.searches;
+    if (kernels) *kernels = g_sp_timing.kernels;
+    g_sp_timing.search_ms = 0.0;
+    g_sp_timing.searches = 0;
+    g_sp_timing.kernels = 0;
+    return APSP_OK;
 }
 
 apsp_status_t apsp_sparse_release(void) {

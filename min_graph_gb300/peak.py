@@ -46,6 +46,9 @@ def _load():
         lib.apsp_peak_addmin.restype = ctypes.c_int
         lib.apsp_peak_variants.argtypes = []
         lib.apsp_peak_variants.restype = ctypes.c_int
+        lib.apsp_peak_l2_read.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        lib.apsp_peak_l2_read.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -60,3 +63,19 @@ def measure(variant: int, blocks: int, threads: int = 256, iters: int = 4096) ->
     return {"variant": variant, "what": VARIANTS[variant], "relax_per_clk_sm": rpc.value,
             "ms": ms.value, "relax": tot.value,
             "relax_per_s": tot.value / (ms.value * 1e-3) if ms.value > 0 else 0.0}
+
+
+def l2_read(nbytes: int = 64 << 20, blocks: int = 0, threads: int = 256, passes: int = 200) -> dict:
+    """L2 read bandwidth (GB/s) over an L2-resident buffer (include/apsp_peak.h).
+    blocks = 0 takes 4 per SM of the current device."""
+    if blocks <= 0:
+        import torch
+
+        blocks = 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    gbs, ms = ctypes.c_double(), ctypes.c_double()
+    rc = _load().apsp_peak_l2_read(int(nbytes), int(blocks), int(threads), int(passes),
+                                   ctypes.byref(gbs), ctypes.byref(ms))
+    if rc != 0:
+        raise RuntimeError(f"apsp_peak_l2_read failed: {rc}")
+    return {"bytes": nbytes, "blocks": blocks, "threads": threads, "passes": passes,
+            "gbs": gbs.value, "ms": ms.value}

@@ -270,3 +270,25 @@ def test_er32768_sampled_sources():
     src = np.random.default_rng(1).choice(n, 64, replace=False).astype(np.int32)
     got = apsp.sssp_delta(rp, col, wt, torch.from_numpy(src).cuda())
     assert_i32_exact(got.cpu().numpy(), oracle.dijkstra_i32(w, src), "er32768 rows")
+
+
+def test_sparse_timing_counts_searches_and_kernels():
+    w = graphgen.er_i32(700, 0.02, 1, 100, seed=3)
+    t = torch.from_numpy(w).cuda()
+    apsp.sparse_timing_read()
+    apsp.sparse_timing_enable(True)
+    try:
+        apsp.solve_sparse(t)
+    finally:
+        apsp.sparse_timing_enable(False)
+    ms, searches, kernels = apsp.sparse_timing_read()
+    assert searches == 1 and ms > 0
+    assert kernels == 6  # count + scan + fill + weight range + partition + search
+    assert apsp.sparse_timing_read() == (0.0, 0, 0)
+
+
+def test_l2_probe_reports_a_bandwidth():
+    import min_graph_gb300.peak as peak
+
+    r = peak.l2_read(8 << 20, passes=4)
+    assert r["gbs"] > 100.0
