@@ -52,8 +52,8 @@
  * every pointer passed in.
  *
  * Limits: n <= APSP_SPARSE_MAX_N.  Each search CTA keeps one source's
- * distances and a bitmap of queued vertices in shared memory, 4.125 bytes
- * per vertex.
+ * distances, a bitmap of queued vertices and the least queued distance per
+ * bitmap word in shared memory, 4.25 bytes per vertex.
  *
  * Thread safety: any host thread may call these.  Sparse calls on one
  * process are serialised by a lock.

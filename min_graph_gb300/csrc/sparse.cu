@@ -239,9 +239,10 @@ struct SpShared {
     int item;
 };
 
-// Shared memory of a search CTA: dist (int32, n) and the queued bitmap.
+// Shared memory of a search CTA: dist (int32, n), the queued bitmap, and
+// per bitmap word the least distance of its queued vertices (wmin).
 __host__ __device__ constexpr size_t sssp_shared_offset(int n) {
-    return ((size_t)n * 4 + (size_t)((n + 31) / 32) * 4 + 15) / 16 * 16;
+    return ((size_t)n * 4 + (size_t)((n + 31) / 32) * 8 + 15) / 16 * 16;
 }
 
 size_t sssp_smem_bytes(int n) { return sssp_shared_offset(n) + sizeof(SpShared); }
@@ -285,7 +286,7 @@ __device__ __forceinline__ int last_lane_at_or_below(int key, int t) {
 template <bool kLight, int kWarps, int kUnroll>
 __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restrict__ rp,
                                           const int32_t* __restrict__ nlight, const int2* __restrict__ arcs,
-                                          int32_t* dist, uint32_t* queued, int warp, int lane) {
+                                          int32_t* dist, uint32_t* queued, int32_t* wmin, int warp, int lane) {
     int32_t best = INT_MAX;
     const int c = __popc(bits);
     int wincl = c;
@@ -342,6 +343,7 @@ __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restri
                 const int u = a[q].x;
                 if (nd < dist[u] && nd < atomicMin(dist + u, nd)) {
                     atomicOr(queued + (u >> 5), 1u << (u & 31));
+                    atomicMin(wmin + (u >> 5), nd);
                     best = min(best, nd);
                 }
             }
@@ -357,7 +359,10 @@ __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restri
 //
 // Lane j of warp w owns bitmap word j * kWarps + w (n <= 1024 * kWarps):
 // it selects that word's queued vertices into its frontier register F and
-// accumulates R (removed from the current bucket) in another register.
+// accumulates R (removed from the current bucket) in another register.  The
+// word's least queued distance (wmin, kept current by the relaxations with
+// an atomic min) lets a selection skip every word with nothing in the
+// bucket without reading its distances.
 // Per bucket: light phases (select the queued vertices below the bucket's
 // upper end hi, relax their light arcs) until a selection comes back empty;
 // that last selection also yields the least queued distance at or above hi.
@@ -370,11 +375,12 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
                   int32_t delta, const long long* __restrict__ h, int32_t* __restrict__ out, long long ldo,
                   int* __restrict__ counter, int* __restrict__ err) {
     constexpr int kWarps = kThreads / 32;
-    constexpr int kUnroll = 2;
+    constexpr int kUnroll = 4;
     extern __shared__ __align__(16) unsigned char sp_smem[];
     const int nw = (n + 31) / 32;
     int32_t* dist = reinterpret_cast<int32_t*>(sp_smem);
-    uint32_t* queued = reinterpret_cast<uint32_t*>(dist + n);  // waiting in some bucket
+    uint32_t* queued = reinterpret_cast<uint32_t*>(dist + n);    // waiting in some bucket
+    int32_t* wmin = reinterpret_cast<int32_t*>(queued + nw);     // least queued distance per word
     SpShared* sh = reinterpret_cast<SpShared*>(sp_smem + sssp_shared_offset(n));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int myword = lane * kWarps + warp;
@@ -392,7 +398,10 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
             continue;
         }
         for (int v = tid; v < n; v += kThreads) dist[v] = kUnreached;
-        for (int i = tid; i < nw; i += kThreads) queued[i] = 0u;
+        for (int i = tid; i < nw; i += kThreads) {
+            queued[i] = 0u;
+            wmin[i] = INT_MAX;
+        }
         if (tid == 0) {
             sh->dmin[0] = INT_MAX;
             sh->dmin[1] = INT_MAX;
@@ -401,6 +410,7 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
         if (tid == 0) {
             dist[src] = 0;
             queued[src >> 5] = 1u << (src & 31);
+            wmin[src >> 5] = 0;
         }
         __syncthreads();
 
@@ -414,26 +424,33 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
                 beyond = INT_MAX;
                 uint32_t fbits = 0u;
                 if (owns) {
-                    uint32_t bits = queued[myword];
-                    const uint32_t all = bits;
-                    while (bits) {
-                        const int b = __ffs(bits) - 1;
-                        bits &= bits - 1;
-                        const int32_t dd = dist[myword * 32 + b];
-                        if (dd < hi)
-                            fbits |= 1u << b;
-                        else
-                            beyond = min(beyond, dd);
+                    const int32_t wm = wmin[myword];
+                    if (wm < hi) {  // else nothing of this word is in the bucket: skip its bits
+                        uint32_t bits = queued[myword];
+                        const uint32_t all = bits;
+                        while (bits) {
+                            const int b = __ffs(bits) - 1;
+                            bits &= bits - 1;
+                            const int32_t dd = dist[myword * 32 + b];
+                            if (dd < hi)
+                                fbits |= 1u << b;
+                            else
+                                beyond = min(beyond, dd);
+                        }
+                        queued[myword] = all & ~fbits;
+                        wmin[myword] = beyond;
+                        rbits |= fbits;
+                    } else {
+                        beyond = wm;
                     }
-                    if (fbits) queued[myword] = all & ~fbits;
-                    rbits |= fbits;
                 }
                 if (!__syncthreads_or(fbits != 0u)) break;
-                expand<true, kWarps, kUnroll>(fbits, rp, nlight, arcs, dist, queued, warp, lane);
+                expand<true, kWarps, kUnroll>(fbits, rp, nlight, arcs, dist, queued, wmin, warp, lane);
                 __syncthreads();
             }
             // heavy arcs of R, once; then the next bucket from the least queued distance
-            const int32_t hbest = expand<false, kWarps, kUnroll>(rbits, rp, nlight, arcs, dist, queued, warp, lane);
+            const int32_t hbest =
+                expand<false, kWarps, kUnroll>(rbits, rp, nlight, arcs, dist, queued, wmin, warp, lane);
             const int32_t next = __reduce_min_sync(0xffffffffu, min(beyond, hbest));
             const int slot = bucket & 1;
             if (lane == 0 && next != INT_MAX) atomicMin(&sh->dmin[slot], next);
