@@ -68,6 +68,10 @@ def _load():
             lib.graphgen_ba_edges.restype = i64
             lib.graphgen_ba_i32.argtypes = [vp, i64, i64, i32, i32, i32, i32, u64]
             lib.graphgen_ba_i32.restype = i64
+            lib.graphgen_rmat_arcs.argtypes = [vp, vp, vp, i64, i64, i32, dbl, dbl, dbl, i32, i32, u64]
+            lib.graphgen_rmat_arcs.restype = None
+            lib.graphgen_csr_from_arcs.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]
+            lib.graphgen_csr_from_arcs.restype = i32
             _lib = lib
     return _lib
 
@@ -165,6 +169,45 @@ def ba_i32(n: int, beta: int, wlo: int, whi: int, seed: int, ld: int | None = No
     if arcs != 2 * beta * (n - beta):
         raise ValueError("bad Barabasi-Albert arguments")
     return out
+
+
+RMAT_ABC = (0.57, 0.19, 0.19)  # Graph500 quadrant probabilities (d = 0.05)
+
+
+def rmat_csr(scale: int, edge_factor: int = 32, wlo: int = 1, whi: int = 1 << 20, seed: int = 6,
+             abc=RMAT_ABC, threads: int | None = None):
+    """R-MAT graph with 2^scale vertices and edge_factor * 2^scale arcs, as
+    CSR (row_ptr int64[n+1], col int32[m], w int32[m]); see gen.c for the
+    recipe (Graph500 quadrant probabilities, scrambled vertex ids, int32
+    weights uniform in [wlo, whi], self-loops and parallel arcs kept)."""
+    if not 1 <= scale <= 30:
+        raise ValueError("scale must be in [1, 30]")
+    n = 1 << scale
+    m = edge_factor * n
+    tail = np.empty(m, dtype=np.int32)
+    head = np.empty(m, dtype=np.int32)
+    wt = np.empty(m, dtype=np.int32)
+    lib = _load()
+    a, b, c = abc
+
+    def arcs(e0, e1):
+        lib.graphgen_rmat_arcs(tail.ctypes.data + 4 * e0, head.ctypes.data + 4 * e0, wt.ctypes.data + 4 * e0,
+                               e0, e1, scale, a, b, c, wlo, whi, seed)
+
+    _rows_parallel(arcs, m, threads)
+    row_ptr = np.empty(n + 1, dtype=np.int64)
+    col = np.empty(m, dtype=np.int32)
+    w = np.empty(m, dtype=np.int32)
+    rc = lib.graphgen_csr_from_arcs(tail.ctypes.data, head.ctypes.data, wt.ctypes.data, m, n,
+                                    row_ptr.ctypes.data, col.ctypes.data, w.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"graphgen_csr_from_arcs failed: {rc}")
+    return row_ptr, col, w
+
+
+def describe_rmat(scale: int, edge_factor: int = 32, wlo: int = 1, whi: int = 1 << 20, seed: int = 6) -> str:
+    return (f"R-MAT scale {scale} (n = {1 << scale}), {edge_factor} arcs per vertex, "
+            f"(a,b,c,d) = (0.57,0.19,0.19,0.05), int32 w in [{wlo},{whi}], seed {seed}")
 
 
 # name -> (kind, n, params, dtype)

@@ -179,3 +179,65 @@ void graphgen_er_potential_i32(int32_t* out, int64_t n, int64_t ld, int64_t row_
         }
     }
 }
+
+/* ---------------- R-MAT (sparse, CSR) ----------------
+ *
+ * The Delta-stepping page measures on R-MAT graphs of scale 17..23 (2^scale
+ * vertices) with 32 arcs per vertex on average.  It names the model but not
+ * its parameters; this recipe takes the usual Graph500 quadrant
+ * probabilities (a, b, c, d) = (0.57, 0.19, 0.19, 0.05).
+ *
+ * Arc e (0 <= e < m) descends `scale` levels of the adjacency matrix: at
+ * level l the draw at stream position e * 64 + l + 1 picks a quadrant, which
+ * fixes one bit of the tail and one of the head.  Its weight is drawn at
+ * position 2^44 + e.  Vertex ids then go through the bijection
+ * v -> (v * 0x9E3779B1 + 0x7F4A7C15) mod 2^scale (odd multiplier), so that
+ * the high-degree vertices do not all sit at the lowest ids.  Self-loops and
+ * parallel arcs are kept: the arc list is what the model draws.
+ *
+ * graphgen_rmat_arcs fills tail/head/weight for arcs [e_begin, e_end).
+ * graphgen_csr_from_arcs is a stable counting sort of those arcs by tail:
+ * row_ptr (n + 1), then col/w in arc order within each row. */
+static inline uint32_t rmat_scramble(uint32_t v, int scale) {
+    const uint32_t mask = scale >= 32 ? 0xFFFFFFFFu : ((1u << scale) - 1u);
+    return (uint32_t)((v * 0x9E3779B1u + 0x7F4A7C15u) & mask);
+}
+
+void graphgen_rmat_arcs(int32_t* tail, int32_t* head, int32_t* weight, int64_t e_begin, int64_t e_end,
+                        int32_t scale, double a, double b, double c, int32_t wlo, int32_t whi, uint64_t seed) {
+    for (int64_t e = e_begin; e < e_end; ++e) {
+        uint32_t u = 0, v = 0;
+        for (int l = 0; l < scale; ++l) {
+            const double r = gen_unit(graphgen_splitmix64_at(seed, (uint64_t)e * 64u + (uint64_t)l + 1u));
+            const uint32_t bu = r >= a + b ? 1u : 0u;           /* quadrants c and d: lower half */
+            const uint32_t bv = (r >= a && r < a + b) || r >= a + b + c ? 1u : 0u;  /* b and d: right half */
+            u = (u << 1) | bu;
+            v = (v << 1) | bv;
+        }
+        const int64_t k = e - e_begin;
+        tail[k] = (int32_t)rmat_scramble(u, scale);
+        head[k] = (int32_t)rmat_scramble(v, scale);
+        weight[k] = gen_int(graphgen_splitmix64_at(seed, (1ULL << 44) + (uint64_t)e), wlo, whi);
+    }
+}
+
+/* Stable counting sort by tail.  row_ptr must hold n + 1 entries. */
+int graphgen_csr_from_arcs(const int32_t* tail, const int32_t* head, const int32_t* weight, int64_t m, int64_t n,
+                           int64_t* row_ptr, int32_t* col, int32_t* w) {
+    memset(row_ptr, 0, sizeof(int64_t) * (size_t)(n + 1));
+    for (int64_t e = 0; e < m; ++e) {
+        if (tail[e] < 0 || tail[e] >= n || head[e] < 0 || head[e] >= n) return -1;
+        row_ptr[tail[e] + 1]++;
+    }
+    for (int64_t v = 0; v < n; ++v) row_ptr[v + 1] += row_ptr[v];
+    int64_t* cur = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n ? n : 1));
+    if (!cur) return -2;
+    memcpy(cur, row_ptr, sizeof(int64_t) * (size_t)n);
+    for (int64_t e = 0; e < m; ++e) {
+        const int64_t p = cur[tail[e]]++;
+        col[p] = head[e];
+        w[p] = weight[e];
+    }
+    free(cur);
+    return 0;
+}

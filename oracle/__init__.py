@@ -19,6 +19,8 @@ diagonal.  Two independent algorithms give it:
                            check (Johnson/Dijkstra page).
   johnson_i32              Johnson's APSP as that page lays it out: negative
                            arc weights allowed, negative cycles reported.
+  dijkstra_csr_i32         the same Dijkstra read from a CSR arc list (for
+                           sparse graphs too large for a dense matrix).
 
 int32 matrices use INF = 0x3FFFFFFF; floating point is computed in double
 with +inf for "no arc".
@@ -87,6 +89,8 @@ def bind(path: str):
     lib.oracle_bellman_ford_i32.restype = i32
     lib.oracle_johnson_i32.argtypes = [vp, i64, i64, vp, i32]
     lib.oracle_johnson_i32.restype = i32
+    lib.oracle_dijkstra_csr_i32.argtypes = [vp, vp, vp, i64, vp, i64, vp, i32]
+    lib.oracle_dijkstra_csr_i32.restype = i32
     return lib
 
 
@@ -199,6 +203,21 @@ class Oracle:
         _check(rc, "johnson_i32")
         return out
 
+    def dijkstra_csr_i32(self, row_ptr: np.ndarray, col: np.ndarray, w: np.ndarray, sources,
+                         threads: int | None = None) -> np.ndarray:
+        """Rows of distances from `sources` on a CSR graph (int64 row_ptr,
+        int32 col and w >= 0); int32 with INF for unreachable."""
+        row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int64)
+        col = np.ascontiguousarray(col, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.int32)
+        n = row_ptr.size - 1
+        src = np.ascontiguousarray(np.asarray(sources, dtype=np.int32))
+        out = np.empty((src.size, n), dtype=np.int32)
+        _check(self.lib.oracle_dijkstra_csr_i32(row_ptr.ctypes.data, col.ctypes.data, w.ctypes.data, n,
+                                                src.ctypes.data, src.size, out.ctypes.data,
+                                                threads or default_threads()), "dijkstra_csr_i32")
+        return out
+
     def bfs_hops_i32(self, w: np.ndarray, src: int) -> np.ndarray:
         w = _as_matrix(w, np.int32)
         hops = np.empty(w.shape[0], dtype=np.int32)
@@ -243,3 +262,7 @@ def bellman_ford_i32(w, src):
 
 def johnson_i32(w, threads=None):
     return default().johnson_i32(w, threads=threads)
+
+
+def dijkstra_csr_i32(row_ptr, col, w, sources, threads=None):
+    return default().dijkstra_csr_i32(row_ptr, col, w, sources, threads=threads)

@@ -422,3 +422,75 @@ int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, in
     free(h);
     return err;
 }
+
+/* ---------------- Dijkstra on a CSR graph ----------------
+ *
+ * The same binary-heap Dijkstra (Johnson/Dijkstra page, the sequential
+ * Dijkstra operators) read straight from a CSR arc list: the arcs leaving u
+ * are row_ptr[u] .. row_ptr[u+1]-1, heads col[], weights w[] (all >= 0).
+ * Self-loops and parallel arcs are allowed.  out (ns x n, int32) gets the
+ * distance from sources[s], INF for unreachable, and distances at or above
+ * INF read as INF.  Returns 0, -1 on bad arguments (including a negative
+ * weight or a head out of range), -2 on allocation failure. */
+static int o_dijkstra_csr_one(const int64_t* row_ptr, const int32_t* col, const int32_t* w, int64_t n,
+                              int64_t src, int64_t* di, unsigned char* settled) {
+    o_heap h = {0, 0, 0, 1};
+    for (int64_t v = 0; v < n; ++v) { di[v] = INT64_MAX; settled[v] = 0; }
+    di[src] = 0;
+    o_item s0 = {0.0, 0, (int32_t)src};
+    if (o_push(&h, s0)) return -2;
+    while (h.size > 0) {
+        o_item it = o_pop(&h);
+        const int64_t u = it.v;
+        if (settled[u]) continue;
+        settled[u] = 1;
+        for (int64_t e = row_ptr[u]; e < row_ptr[u + 1]; ++e) {
+            const int64_t v = col[e];
+            const int64_t nd = di[u] + w[e];
+            if (nd < di[v]) {
+                di[v] = nd;
+                o_item x = {0.0, nd, (int32_t)v};
+                if (o_push(&h, x)) { free(h.a); return -2; }
+            }
+        }
+    }
+    free(h.a);
+    return 0;
+}
+
+int oracle_dijkstra_csr_i32(const int64_t* row_ptr, const int32_t* col, const int32_t* w, int64_t n,
+                            const int32_t* sources, int64_t ns, int32_t* out, int threads) {
+    if (n <= 0 || ns < 0 || !row_ptr || !sources || !out || row_ptr[0] != 0) return -1;
+    for (int64_t v = 0; v < n; ++v)
+        if (row_ptr[v + 1] < row_ptr[v]) return -1;
+    const int64_t m = row_ptr[n];
+    if (m > 0 && (!col || !w)) return -1;
+    for (int64_t e = 0; e < m; ++e)
+        if (w[e] < 0 || col[e] < 0 || col[e] >= n) return -1;
+    for (int64_t s = 0; s < ns; ++s)
+        if (sources[s] < 0 || sources[s] >= n) return -1;
+    int err = 0;
+    (void)threads;
+#pragma omp parallel num_threads(threads > 0 ? threads : 1) if (threads > 1)
+    {
+        int64_t* di = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+        unsigned char* st = (unsigned char*)malloc((size_t)n);
+        if (!di || !st) {
+#pragma omp atomic write
+            err = -2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t s = 0; s < ns; ++s) {
+                if (o_dijkstra_csr_one(row_ptr, col, w, n, sources[s], di, st)) {
+#pragma omp atomic write
+                    err = -2;
+                    continue;
+                }
+                int32_t* row = out + s * n;
+                for (int64_t v = 0; v < n; ++v) row[v] = (int32_t)(di[v] < O_INF ? di[v] : O_INF);
+            }
+        }
+        free(di); free(st);
+    }
+    return err;
+}

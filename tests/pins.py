@@ -331,8 +331,51 @@ def check_negative_weights(orc) -> list[str]:
     return bad
 
 
+def random_multigraph(seed: int):
+    """A small CSR multigraph: parallel arcs (up to three per ordered pair)
+    and self-loops, weights in [0, 30]."""
+    rng = np.random.default_rng(10_000 + seed)
+    n = int(rng.integers(1, 8))
+    m = int(rng.integers(0, 4 * n * n + 1))
+    tail = rng.integers(0, n, m)
+    head = rng.integers(0, n, m)
+    wt = rng.integers(0, 31, m).astype(np.int32)
+    order = np.argsort(tail, kind="stable")
+    row_ptr = np.concatenate([[0], np.cumsum(np.bincount(tail, minlength=n))]).astype(np.int64)
+    return n, row_ptr, head[order].astype(np.int32), wt[order], tail[order]
+
+
+def check_dijkstra_csr(orc) -> list[str]:
+    """The CSR Dijkstra on multigraphs against brute force over simple paths
+    (parallel arcs reduce to their lightest, self-loops never help), against
+    the dense Dijkstra on the same graphs, and the directed-path closed form."""
+    bad = []
+    for seed in range(40):
+        n, row_ptr, col, wt, tail = random_multigraph(seed)
+        dense = np.full((n, n), INF, dtype=np.int64)
+        np.fill_diagonal(dense, 0)
+        off = tail != col
+        np.minimum.at(dense, (tail[off], col[off]), wt[off])
+        dense = dense.astype(np.int32)
+        ref = brute_force(dense, integer=True)
+        got = orc.dijkstra_csr_i32(row_ptr, col, wt, np.arange(n))
+        if not np.array_equal(got.astype(np.int64), ref):
+            bad.append(f"dijkstra_csr seed {seed}: differs from brute force")
+        if not np.array_equal(got, orc.dijkstra_i32(dense, np.arange(n))):
+            bad.append(f"dijkstra_csr seed {seed}: differs from the dense Dijkstra")
+    n = 50  # directed path 0 -> 1 -> ... -> 49: prefix sums
+    wts = np.arange(1, n, dtype=np.int32) * 3
+    row_ptr = np.concatenate([np.arange(n, dtype=np.int64), [n - 1]])
+    got = orc.dijkstra_csr_i32(row_ptr, np.arange(1, n, dtype=np.int32), wts, [0, 10])
+    pref = np.concatenate([[0], np.cumsum(wts)])
+    if not (np.array_equal(got[0], pref) and np.array_equal(got[1, 10:], pref[10:] - pref[10])
+            and np.all(got[1, :10] == INF)):
+        bad.append("dijkstra_csr: directed path closed form")
+    return bad
+
+
 ALL_CHECKS = (check_golden, check_brute_force, check_closed_forms, check_invariants, check_fw_vs_dijkstra,
-              check_negative_weights)
+              check_negative_weights, check_dijkstra_csr)
 
 
 def run_all(orc) -> list[str]:

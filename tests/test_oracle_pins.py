@@ -81,6 +81,27 @@ def test_networkx_third_opinion():
         assert np.array_equal(oracle.fw_i32(w).astype(np.int64), ref)
 
 
+def test_dijkstra_csr():
+    bad = pins.check_dijkstra_csr(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
+def test_generator_rmat_shape():
+    # 2^scale vertices, 32 arcs per vertex, deterministic, weights in range,
+    # a heavy-tailed out-degree (R-MAT quadrant probabilities 0.57/0.19/0.19/0.05)
+    row_ptr, col, w = graphgen.rmat_csr(12, whi=1000)
+    n = 1 << 12
+    assert row_ptr.shape == (n + 1,) and row_ptr[0] == 0 and row_ptr[-1] == 32 * n
+    assert np.all(np.diff(row_ptr) >= 0) and col.min() >= 0 and col.max() < n
+    assert w.min() >= 1 and w.max() <= 1000
+    deg = np.diff(row_ptr)
+    assert deg.max() > 20 * deg.mean() and np.mean(deg == 0) > 0.1
+    r2 = graphgen.rmat_csr(12, whi=1000)
+    assert all(np.array_equal(a, b) for a, b in zip((row_ptr, col, w), r2))
+    # arcs of a row keep the draw order: the counting sort is stable
+    assert np.array_equal(graphgen.rmat_csr(12, whi=1000, threads=1)[1], col)
+
+
 def test_generator_splitmix64_known_value():
     # First output of SplitMix64 seeded with 0 (published reference value).
     assert graphgen.splitmix64_at(0, 1) == 0xE220A8397B1DCDAF
@@ -147,6 +168,8 @@ MUTANTS = [
      "h[u] + w[u * ld + v] < h[v]) {", "h[u] + w[u * ld + v] < h[v] - 2000000000) {"),
     ("bellman-ford: source distance not zero",
      "out[src] = 0;", "out[src] = 1;"),
+    ("dijkstra_csr: last arc of every row skipped",
+     "for (int64_t e = row_ptr[u]; e < row_ptr[u + 1]; ++e) {", "for (int64_t e = row_ptr[u]; e < row_ptr[u + 1] - 1; ++e) {"),
 ]
 
 
