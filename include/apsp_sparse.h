@@ -110,6 +110,22 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
                                   int32_t* out, int ldo, apsp_stream_t stream);
 
 /*
+ * apsp_sssp_i32 -- one Delta-stepping search from `source` using the whole
+ * GPU, for graphs of any size the device memory holds (the Delta-stepping
+ * page's single-source setting; no shared-memory limit on n).  CSR as above,
+ * weights >= 0 (a negative weight returns APSP_EINVAL), fewer than 2^31 arcs.
+ *   dist   device int32[n], 16-byte aligned: the distances from source, INF
+ *          for unreachable.  It also serves as the search's working array.
+ *   delta  as for apsp_solve_sparse_i32.
+ * The search is one cooperative launch whose CTAs meet at grid barriers.
+ * Every barrier wait is bounded (2 s); one that runs out returns
+ * APSP_ETIMEOUT, and dist is then undefined.  Workspace: about 8 bytes per
+ * arc plus 5.25 bytes per vertex, kept per device like the rest.
+ */
+apsp_status_t apsp_sssp_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n, int source,
+                            int32_t delta, int32_t* dist, apsp_stream_t stream);
+
+/*
  * apsp_csr_count_i32 / apsp_csr_fill_i32 -- build the CSR of a dense int32
  * device matrix, with the arcs as defined above.
  * count: writes row_ptr (device, int64[n + 1]), and the arc count m to

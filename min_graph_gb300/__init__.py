@@ -100,6 +100,8 @@ def load():
         lib.apsp_csr_fill_i32.restype = i32
         lib.apsp_sparse_release.argtypes = []
         lib.apsp_sparse_release.restype = i32
+        lib.apsp_sssp_i32.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+        lib.apsp_sssp_i32.restype = i32
         lib.apsp_sparse_timing_enable.argtypes = [i32]
         lib.apsp_sparse_timing_enable.restype = i32
         lib.apsp_sparse_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
@@ -352,6 +354,27 @@ def sssp_delta(row_ptr, col_idx, w, sources, delta: int = 0, out=None, stream=No
         _check(lib.apsp_sssp_delta_i32(row_ptr.data_ptr(), col_idx.data_ptr(), w.data_ptr(), n,
                                        sources.data_ptr(), nsrc, int(delta), out.data_ptr(), ldo, s),
                "apsp_sssp_delta_i32")
+    return out
+
+
+def sssp(row_ptr, col_idx, w, source: int, delta: int = 0, out=None, stream=None):
+    """One Delta-stepping search from `source` over the whole GPU on a CSR
+    graph with weights >= 0 (include/apsp_sparse.h, apsp_sssp_i32).  Returns
+    (or fills) an int32 CUDA tensor of n distances, INF for unreachable.
+    Blocks until done."""
+    import torch
+
+    lib = load()
+    n = _csr_args(row_ptr, col_idx, w)
+    if out is None:
+        out = torch.empty(max(n, 1), dtype=torch.int32, device=row_ptr.device)[:n]
+    if out.dtype != torch.int32 or not out.is_cuda or out.dim() != 1 or out.numel() != n or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int32 CUDA tensor of n entries")
+    s = _stream_handle(row_ptr, stream)
+    with torch.cuda.device(row_ptr.device):
+        _check(lib.apsp_sssp_i32(row_ptr.data_ptr(), col_idx.data_ptr() if col_idx.numel() else None,
+                                 w.data_ptr() if w.numel() else None, n, int(source), int(delta),
+                                 out.data_ptr(), s), "apsp_sssp_i32")
     return out
 
 

@@ -38,6 +38,7 @@
 
 #include "../../include/apsp.h"
 #include "../../include/apsp_sparse.h"
+#include "tma.cuh"
 
 namespace apsp {
 void set_last_cuda_error(int e);  // defined with apsp_last_cuda_error()
@@ -472,6 +473,369 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
     }
 }
 
+// ------------------------------------------------------------------ grid-wide Delta-stepping
+
+// One search over the whole GPU, for graphs whose distances do not fit a
+// CTA's shared memory (the Delta-stepping page's single-source setting).
+// The same buckets, light phases and heavy phase as above, with the state in
+// global memory:
+//   dist (the caller's output array), queued and wmin as in the CTA search,
+//   front (this phase's frontier) and rset (R) bitmaps.
+// Lane j of global warp g owns bitmap words (s * G + g) * 32 + j, s = 0, 1,
+// ... (G warps in the grid), so a warp's lanes hold 32 adjacent words.
+// Phases are separated by a grid barrier (below) that also reduces an OR
+// (is the bucket empty?) and a MIN (the next bucket) over all CTAs.  State
+// that other SMs write is read through L2 (ld.global.cg), never from a stale
+// L1 line.  Arc data is read-only and goes through the read-only path.  A
+// vertex with more than kGridBig arcs in the phase is not walked by its warp
+// alone: it goes to a per-CTA list that all warps of the CTA share out in
+// 128-arc pieces after their own batches.
+
+constexpr int kGridThreads = 512;
+constexpr int kGridWarps = kGridThreads / 32;
+constexpr int kGridBig = 1024;
+constexpr int kGridBigCap = 128;
+
+struct GridCtrl {
+    int any[3];          // OR slots, by barrier index mod 3
+    int mn[3];           // MIN slots
+    unsigned arrive;     // barrier arrivals
+    unsigned gen;        // barrier generation
+    int err;             // 1: a barrier wait ran out
+    int pad[7];
+};
+
+struct GridArgs {
+    const int64_t* rp;
+    const int32_t* nlight;
+    const int2* arcs;
+    int n, nw;
+    int32_t delta;
+    int32_t* dist;
+    uint32_t* queued;
+    int32_t* wmin;
+    uint32_t* front;
+    uint32_t* rset;
+    GridCtrl* ctrl;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ int32_t ld_cg_i32(const int32_t* p) { return __ldcg(p); }
+
+// Grid barrier with an OR and a MIN reduction; slot k % 3 of the control
+// block holds barrier k's reductions, and CTA 0 clears slot (k + 2) % 3 once
+// past barrier k (every CTA has read that slot, used by barrier k - 1, and
+// none writes it before barrier k + 2).  Waits are bounded: after timeout_ns
+// the CTA sets ctrl->err; every waiting CTA sees it and leaves.  Returns
+// false when the search must stop.
+__device__ bool grid_reduce(const GridArgs& a, int& k, int any_in, int32_t min_in, int& any_out,
+                            int32_t& min_out) {
+    __shared__ int s_min, s_any, s_err;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) s_min = INT_MAX;
+    const int any_b = __syncthreads_or(any_in);
+    const int32_t wm = __reduce_min_sync(0xffffffffu, min_in);
+    if (lane == 0 && wm != INT_MAX) atomicMin(&s_min, wm);
+    __syncthreads();
+    if (tid == 0) {
+        GridCtrl* c = a.ctrl;
+        const int slot = k % 3;
+        if (any_b) atomicOr(&c->any[slot], 1);
+        if (s_min != INT_MAX) atomicMin(&c->mn[slot], s_min);
+        const unsigned g0 = *reinterpret_cast<volatile unsigned*>(&c->gen);
+        __threadfence();
+        const unsigned arrived = atomicAdd(&c->arrive, 1u) + 1u;
+        if (arrived == gridDim.x) {
+            atomicExch(&c->arrive, 0u);
+            __threadfence();
+            atomicAdd(&c->gen, 1u);
+        } else {
+            const unsigned long long t0 = apsp::global_timer_ns();
+            unsigned spins = 0;
+            while (*reinterpret_cast<volatile unsigned*>(&c->gen) == g0) {
+                if (*reinterpret_cast<volatile int*>(&c->err)) break;
+                if ((++spins & 255u) == 0u && apsp::global_timer_ns() - t0 > a.timeout_ns) {
+                    atomicExch(&c->err, 1);
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+        s_any = *reinterpret_cast<volatile int*>(&c->any[slot]);
+        s_min = *reinterpret_cast<volatile int*>(&c->mn[slot]);
+        s_err = *reinterpret_cast<volatile int*>(&c->err);
+        if (blockIdx.x == 0) {
+            const int r = (k + 2) % 3;
+            c->any[r] = 0;
+            c->mn[r] = INT_MAX;
+        }
+    }
+    __syncthreads();
+    any_out = s_any;
+    min_out = s_min;
+    const bool ok = s_err == 0;
+    __syncthreads();  // s_* are rewritten by the next call
+    ++k;
+    return ok;
+}
+
+struct GridBig {
+    int4 e[kGridBigCap];  // (dv, begin, count, -)
+    int count;
+};
+
+// Relax `cnt` arcs from `beg` for a vertex at distance dv, 32 lanes of a warp
+// striding over them, up to 4 loads in flight.
+__device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int beg, int cnt, uint32_t dv,
+                                             int32_t* dist, uint32_t* queued, int32_t* wmin, int lane) {
+    int32_t best = INT_MAX;
+    for (int o = 0; o < cnt; o += 128) {
+        int2 x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int t = o + q * 32 + lane;
+            x[q] = t < cnt ? __ldg(arcs + beg + t) : make_int2(0, -1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (x[q].y < 0) continue;
+            const uint32_t s = dv + (uint32_t)x[q].y;
+            const int32_t nd = s >= (uint32_t)kUnreached ? kUnreached : (int32_t)s;
+            const int u = x[q].x;
+            if (nd < ld_cg_i32(dist + u) && nd < atomicMin(dist + u, nd)) {
+                atomicOr(queued + (u >> 5), 1u << (u & 31));
+                atomicMin(wmin + (u >> 5), nd);
+                best = min(best, nd);
+            }
+        }
+    }
+    return best;
+}
+
+// Relax the light (kLight) or heavy arcs of every vertex in the bitmap `set`
+// (global), clearing it.  Batches of 32 vertices as in the CTA search; a
+// vertex with more than kGridBig arcs goes to the CTA's list `big` (its warp
+// walks it itself when the list is full), and the CTA's warps share out the
+// list once all batches are done.
+template <bool kLight>
+__device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
+    int32_t best = INT_MAX;
+    for (int s = 0;; ++s) {
+        const long long wbase = ((long long)s * G + gw) * 32;
+        if (wbase >= a.nw) break;  // warp-uniform
+        const int i = (int)wbase + lane;
+        uint32_t bits = 0u;
+        if (i < a.nw) {
+            bits = ld_cg_u32(set + i);
+            if (bits) set[i] = 0u;
+        }
+        const int c = __popc(bits);
+        int wincl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+            if (lane >= o) wincl += y;
+        }
+        const int members = __shfl_sync(0xffffffffu, wincl, 31);
+        const int wexcl = wincl - c;
+        for (int b0 = 0; b0 < members; b0 += 32) {
+            const int g = b0 + lane;
+            const int j = last_lane_at_or_below(wexcl, g);
+            const uint32_t wbits = __shfl_sync(0xffffffffu, bits, j);
+            const int wstart = __shfl_sync(0xffffffffu, wexcl, j);
+            int beg = 0, cnt = 0;
+            uint32_t dv = 0;
+            if (g < members) {
+                const int v = ((int)wbase + j) * 32 + kth_set_bit(wbits, g - wstart);
+                const int r0 = (int)__ldg(a.rp + v), nl = __ldg(a.nlight + v);
+                if (kLight) {
+                    beg = r0;
+                    cnt = nl;
+                } else {
+                    beg = r0 + nl;
+                    cnt = (int)__ldg(a.rp + v + 1) - r0 - nl;
+                }
+                dv = (uint32_t)ld_cg_i32(a.dist + v);
+                if (cnt > kGridBig) {
+                    const int slot = atomicAdd(&big.count, 1);
+                    if (slot < kGridBigCap) {
+                        big.e[slot] = make_int4((int)dv, beg, cnt, 0);
+                        cnt = 0;
+                    }
+                }
+            }
+            const uint32_t heavy = __ballot_sync(0xffffffffu, cnt > kGridBig);  // list full: walk here
+            for (uint32_t hb = heavy; hb; hb &= hb - 1) {
+                const int src = __ffs(hb) - 1;
+                best = min(best, relax_run(a.arcs, __shfl_sync(0xffffffffu, beg, src),
+                                           __shfl_sync(0xffffffffu, cnt, src),
+                                           __shfl_sync(0xffffffffu, dv, src), a.dist, a.queued, a.wmin, lane));
+            }
+            if (cnt > kGridBig) cnt = 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            const int excl = incl - cnt;
+            for (int base = 0; base < total; base += 128) {
+                int2 x[4];
+                uint32_t d[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int t = base + q * 32 + lane;
+                    const int pos = last_lane_at_or_below(excl, t);
+                    const int e = __shfl_sync(0xffffffffu, beg, pos) + t - __shfl_sync(0xffffffffu, excl, pos);
+                    d[q] = __shfl_sync(0xffffffffu, dv, pos);
+                    x[q] = t < total ? __ldg(a.arcs + e) : make_int2(0, -1);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (x[q].y < 0) continue;
+                    const uint32_t sum = d[q] + (uint32_t)x[q].y;
+                    const int32_t nd = sum >= (uint32_t)kUnreached ? kUnreached : (int32_t)sum;
+                    const int u = x[q].x;
+                    if (nd < ld_cg_i32(a.dist + u) && nd < atomicMin(a.dist + u, nd)) {
+                        atomicOr(a.queued + (u >> 5), 1u << (u & 31));
+                        atomicMin(a.wmin + (u >> 5), nd);
+                        best = min(best, nd);
+                    }
+                }
+            }
+        }
+    }
+    // the CTA's big vertices, in 128-arc pieces shared out over its warps
+    __syncthreads();
+    const int nbig = min(big.count, kGridBigCap);
+    int piece = 0;
+    for (int b = 0; b < nbig; ++b) {
+        const int4 e = big.e[b];
+        for (int o = 0; o < e.z; o += 128, ++piece) {
+            if (piece % kGridWarps != warp) continue;
+            best = min(best, relax_run(a.arcs, e.y + o, min(128, e.z - o), (uint32_t)e.x, a.dist, a.queued,
+                                       a.wmin, lane));
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) big.count = 0;
+    return best;
+}
+
+__global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) {
+    __shared__ GridBig big;
+    if (threadIdx.x == 0) big.count = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
+    int k = 0;  // barrier index, the same in every CTA
+    int32_t dmin = 0;
+    for (;;) {  // buckets
+        const long long hi_ll = ((long long)(dmin / a.delta) + 1) * a.delta;
+        const int32_t hi = hi_ll >= kUnreached ? kUnreached : (int32_t)hi_ll;
+        int32_t beyond;
+        for (;;) {  // light phases
+            beyond = INT_MAX;
+            int any = 0;
+            for (int s = 0;; ++s) {
+                const long long wbase = ((long long)s * G + gw) * 32;
+                if (wbase >= a.nw) break;
+                const int i = (int)wbase + lane;
+                if (i >= a.nw) continue;
+                const int32_t wm = ld_cg_i32(a.wmin + i);
+                if (wm >= hi) {
+                    beyond = min(beyond, wm);
+                    continue;
+                }
+                const uint32_t all = ld_cg_u32(a.queued + i);
+                uint32_t sel = 0u;
+                int32_t rem = INT_MAX;
+                const int vb = i * 32;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {  // the word's distances, 4 at a time where any is queued
+                    const uint32_t nib = (all >> (q * 4)) & 0xFu;
+                    if (nib == 0u) continue;
+                    int32_t d4[4];
+                    if (vb + q * 4 + 3 < a.n) {
+                        const int4 v4 = __ldcg(reinterpret_cast<const int4*>(a.dist + vb + q * 4));
+                        d4[0] = v4.x;
+                        d4[1] = v4.y;
+                        d4[2] = v4.z;
+                        d4[3] = v4.w;
+                    } else {  // the ragged end of the array
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            d4[c] = vb + q * 4 + c < a.n ? ld_cg_i32(a.dist + vb + q * 4 + c) : INT_MAX;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (!((nib >> c) & 1u)) continue;
+                        if (d4[c] < hi)
+                            sel |= 1u << (q * 4 + c);
+                        else
+                            rem = min(rem, d4[c]);
+                    }
+                }
+                a.queued[i] = all & ~sel;
+                a.wmin[i] = rem;
+                beyond = min(beyond, rem);
+                if (sel) {
+                    a.front[i] = sel;
+                    a.rset[i] = ld_cg_u32(a.rset + i) | sel;
+                    any = 1;
+                }
+            }
+            int any_g;
+            int32_t unused;
+            if (!grid_reduce(a, k, any, INT_MAX, any_g, unused)) return;
+            if (!any_g) break;
+            expand_grid<true>(a, a.front, big);
+            if (!grid_reduce(a, k, 0, INT_MAX, any_g, unused)) return;
+        }
+        const int32_t hbest = expand_grid<false>(a, a.rset, big);
+        int any_g;
+        int32_t next;
+        if (!grid_reduce(a, k, 0, min(beyond, hbest), any_g, next)) return;
+        if (next == INT_MAX) break;
+        dmin = next;
+    }
+}
+
+// dist <- kUnreached everywhere but the source, the bitmaps cleared, the
+// control block reset.
+__global__ void grid_init_kernel(GridArgs a, int src) {
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long v = t; v < a.n; v += stride) a.dist[v] = v == src ? 0 : kUnreached;
+    for (long long i = t; i < a.nw; i += stride) {
+        a.queued[i] = i == (src >> 5) ? 1u << (src & 31) : 0u;
+        a.wmin[i] = i == (src >> 5) ? 0 : INT_MAX;
+        a.front[i] = 0u;
+        a.rset[i] = 0u;
+    }
+    if (t == 0) {
+        GridCtrl* c = a.ctrl;
+        for (int s = 0; s < 3; ++s) {
+            c->any[s] = 0;
+            c->mn[s] = INT_MAX;
+        }
+        c->arrive = 0u;
+        c->gen = 0u;
+        c->err = 0;
+    }
+}
+
+// Unreached and saturated distances read INF.
+__global__ void grid_finish_kernel(int32_t* dist, int n) {
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += (long long)gridDim.x * blockDim.x)
+        if (dist[v] >= kInf) dist[v] = kInf;
+}
+
 // ------------------------------------------------------------------ host side
 
 struct DevBuf {
@@ -480,7 +844,7 @@ struct DevBuf {
 };
 
 struct SparseState {
-    DevBuf rp, body, work;
+    DevBuf rp, body, work, grid;
 };
 
 std::mutex g_sp_mu;
@@ -787,9 +1151,123 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
     return APSP_OK;
 }
 
+// Grid-search buffer: [ctrl 256 B | flags 256 B | nlight | queued | wmin |
+// front | rset | arcs], each section 256-byte aligned.
+size_t grid_bytes(int n, long long m) {
+    const size_t nw = (size_t)(n + 31) / 32;
+    return 512 + align256((size_t)n * 4) + 4 * align256(nw * 4) + align256((size_t)(m > 0 ? m : 1) * 8);
+}
+
+apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m, int src,
+                          int32_t delta, int32_t* dist, char* buf, cudaStream_t s) {
+    const size_t nw = (size_t)(n + 31) / 32;
+    GridArgs a;
+    a.ctrl = reinterpret_cast<GridCtrl*>(buf);
+    int* flags = reinterpret_cast<int*>(buf + 256);  // [0..2] weight range, [4] row_ptr check
+    size_t off = 512;
+    int32_t* nlight = reinterpret_cast<int32_t*>(buf + off);
+    off += align256((size_t)n * 4);
+    a.queued = reinterpret_cast<uint32_t*>(buf + off);
+    off += align256(nw * 4);
+    a.wmin = reinterpret_cast<int32_t*>(buf + off);
+    off += align256(nw * 4);
+    a.front = reinterpret_cast<uint32_t*>(buf + off);
+    off += align256(nw * 4);
+    a.rset = reinterpret_cast<uint32_t*>(buf + off);
+    off += align256(nw * 4);
+    int2* arcs = reinterpret_cast<int2*>(buf + off);
+    a.rp = rp;
+    a.nlight = nlight;
+    a.arcs = arcs;
+    a.n = n;
+    a.nw = (int)nw;
+    a.dist = dist;
+    a.timeout_ns = 2000000000ull;
+
+    apsp_status_t rc = check_row_ptr(rp, n, flags + 4, s);
+    if (rc != APSP_OK) return rc;
+    int lo = 0, hi = 0, bad = 0;
+    rc = weight_range(w, col, m, n, flags, s, &lo, &hi, &bad);
+    if (rc != APSP_OK) return rc;
+    if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
+    if (delta <= 0) delta = default_delta(n, m, hi);
+    a.delta = delta;
+
+    int dev = 0, sms = 0, coop = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_grid_kernel, kGridThreads, 0);
+    if (e != cudaSuccess) return sp_fail(e);
+    if (!coop || per_sm < 1) return APSP_EUNSUPPORTED;
+    const int grid = sms * min(per_sm, 2);
+
+    partition_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, delta, arcs, nlight);
+    grid_init_kernel<<<sms * 4, 256, 0, s>>>(a, src);
+    count_kernel(2);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    if (g_sp_timing.enabled) {
+        e = cudaEventCreate(&ev[0]);
+        if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[0], s);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t x : ev)
+                if (x) cudaEventDestroy(x);
+            return sp_fail(e);
+        }
+    }
+    void* params[] = {&a};
+    e = cudaLaunchCooperativeKernel((const void*)sssp_grid_kernel, dim3(grid), dim3(kGridThreads), params, 0, s);
+    count_kernel();
+    if (e == cudaSuccess && ev[1]) e = cudaEventRecord(ev[1], s);
+    if (e == cudaSuccess) {
+        grid_finish_kernel<<<sms * 4, 256, 0, s>>>(dist, n);
+        count_kernel();
+        e = cudaGetLastError();
+    }
+    int err = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&err, &a.ctrl->err, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && ev[1]) {
+        float t = 0.f;
+        e = cudaEventElapsedTime(&t, ev[0], ev[1]);
+        if (e == cudaSuccess) {
+            g_sp_timing.search_ms += t;
+            g_sp_timing.searches += 1;
+        }
+    }
+    for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+    if (e != cudaSuccess) return sp_fail(e);
+    return err ? APSP_ETIMEOUT : APSP_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+apsp_status_t apsp_sssp_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n, int source,
+                            int32_t delta, int32_t* dist, apsp_stream_t stream) {
+    if (n < 0 || (n > 0 && (row_ptr == nullptr || dist == nullptr)) || (n > 0 && (source < 0 || source >= n)))
+        return APSP_EINVAL;
+    if (n == 0) return APSP_OK;
+    if (reinterpret_cast<uintptr_t>(dist) % 16 != 0) return APSP_EINVAL;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    SparseState* st = sp_state();
+    if (!st) return APSP_ECUDA;
+    long long m = 0;
+    apsp_status_t rc = read_m(row_ptr, n, &m, s);
+    if (rc != APSP_OK) return rc;
+    if (m < 0 || m >= (long long)INT_MAX || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
+    rc = grow(st->grid, grid_bytes(n, m));
+    if (rc != APSP_OK) return rc;
+    return grid_search(row_ptr, col_idx, w, n, m, source, delta, dist, static_cast<char*>(st->grid.p), s);
+}
+
 
 apsp_status_t apsp_csr_count_i32(const int32_t* dist, int n, int ld, int64_t* row_ptr, long long* m_out,
                                  apsp_stream_t stream) {
@@ -928,13 +1406,13 @@ apsp_status_t apsp_sparse_release(void) {
     apsp_status_t rc = APSP_OK;
     for (size_t dev = 0; dev < g_sp.size(); ++dev) {
         SparseState& st = g_sp[dev];
-        if (!st.rp.p && !st.body.p && !st.work.p) continue;
+        if (!st.rp.p && !st.body.p && !st.work.p && !st.grid.p) continue;
         if (cudaSetDevice((int)dev) != cudaSuccess) {
             rc = APSP_ECUDA;
             continue;
         }
         cudaDeviceSynchronize();
-        for (DevBuf* b : {&st.rp, &st.body, &st.work}) {
+        for (DevBuf* b : {&st.rp, &st.body, &st.work, &st.grid}) {
             if (b->p) cudaFree(b->p);
             b->p = nullptr;
             b->bytes = 0;

@@ -94,6 +94,11 @@ def test_sparse_bad_arguments_rejected_without_cuda(libs):
     assert lib.apsp_csr_count_i32(fake, 4, 3, fake, ctypes.byref(m), None) == apsp.EINVAL
     assert lib.apsp_csr_fill_i32(fake, 4, 4, fake, None, fake, None) == apsp.EINVAL
     assert lib.apsp_csr_fill_i32(None, 0, 0, None, None, None, None) == apsp.OK
+    assert lib.apsp_sssp_i32(None, None, None, 0, 0, 0, None, None) == apsp.OK
+    assert lib.apsp_sssp_i32(fake, fake, fake, 5, 5, 0, fake, None) == apsp.EINVAL    # source >= n
+    assert lib.apsp_sssp_i32(fake, fake, fake, 5, -1, 0, fake, None) == apsp.EINVAL   # source < 0
+    assert lib.apsp_sssp_i32(fake, fake, fake, 5, 0, 0, None, None) == apsp.EINVAL    # no output
+    assert lib.apsp_sssp_i32(fake, fake, fake, 5, 0, 0, ctypes.c_void_p(0x1004), None) == apsp.EINVAL  # misaligned
 
 
 def test_python_binding_rejects_non_cuda():
