@@ -25,6 +25,14 @@ directly.  Its roofline is the search kernel's arc stream (8 bytes per
 packed arc and 20 per vertex range, per source) against the L2 read
 bandwidth measured in the same run; the CPU baseline and the reference arm
 time the oracle's binary-heap Dijkstra from a sample of sources.
+
+--algo sssp measures the grid-wide single-source Delta-stepping search
+(min_graph_gb300.sssp) on an R-MAT graph of 2^scale vertices and 32 arcs per
+vertex, as the Delta-stepping page does: one step is one search from a
+seeded random source, and the metric is traversed edges per second (m /
+search time).  Its roofline is HBM: 8 bytes per arc and 16 per vertex per
+search against the measured copy bandwidth.  The CPU baseline and the
+reference arm time the oracle's CSR Dijkstra from one source.
 """
 from __future__ import annotations
 
@@ -60,7 +68,8 @@ def parse():
     ap.add_argument("--workload", default="ba16384", choices=sorted(graphgen.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--algo", choices=["fw", "johnson"], default="fw")
+    ap.add_argument("--algo", choices=["fw", "johnson", "sssp"], default="fw")
+    ap.add_argument("--scale", type=int, default=22, help="R-MAT scale for --algo sssp")
     ap.add_argument("--delta", type=int, default=0, help="Delta for --algo johnson (0: the library's default)")
     return ap.parse_args()
 
@@ -607,9 +616,182 @@ def ours_johnson(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ single-source arm
+
+SSSP_METRIC = "SSSP traversed edges/s (m/time), grid-wide Delta-stepping on R-MAT, 1 GPU"
+
+
+def sssp_sources(n: int, count: int, row_ptr: np.ndarray) -> np.ndarray:
+    """Seeded random sources with at least one out-arc (a source without one
+    traverses nothing)."""
+    rng = np.random.default_rng(17)
+    deg = np.diff(row_ptr)
+    out = []
+    while len(out) < count:
+        v = int(rng.integers(0, n))
+        if deg[v] > 0:
+            out.append(v)
+    return np.array(out, dtype=np.int32)
+
+
+def reference_sssp(args, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    row_ptr, col, w = graphgen.rmat_csr(args.scale)
+    n, m = row_ptr.size - 1, int(row_ptr[-1])
+    src = sssp_sources(n, args.warmup + args.steps, row_ptr)
+    secs = []
+    for q, s in enumerate(src):
+        t0 = time.perf_counter()
+        oracle.dijkstra_csr_i32(row_ptr, col, w, [int(s)], threads=1)
+        if q >= args.warmup:
+            secs.append(time.perf_counter() - t0)
+    value = m * len(secs) / sum(secs)
+    sample = f"the oracle's binary-heap Dijkstra on the CSR graph, one source per step, 1 thread"
+    line = {
+        "impl": "reference", "metric": SSSP_METRIC, "value": value, "unit": "TEPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(secs) / len(secs) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"rmat{args.scale}", "n": n, "m": m, "graph": graphgen.describe_rmat(args.scale),
+                   "algo": "sssp", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TEPS", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TEPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def ours_sssp(args, rank, world, local):
+    import torch
+
+    import min_graph_gb300 as apsp
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    row_ptr, col, w = graphgen.rmat_csr(args.scale)
+    n, m = row_ptr.size - 1, int(row_ptr[-1])
+    stream = torch.cuda.current_stream(dev)
+    # the graph is prepared once (checked and partitioned against Delta), as
+    # the page builds its CSR once; each step is one search on it
+    graph = apsp.SsspGraph(*[torch.from_numpy(a).to(dev) for a in (row_ptr, col, w)], delta=args.delta)
+    delta_used = graph.info()[2]
+    out = torch.empty(n, dtype=torch.int32, device=dev)
+    src = sssp_sources(n, args.warmup + args.steps, row_ptr)
+    for s in src[:args.warmup]:
+        graph.search(int(s), out=out, stream=stream)
+    apsp.sparse_timing_read()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clocks:
+        apsp.sparse_timing_enable(True)
+        for k, s in enumerate(src[args.warmup:]):
+            starts[k].record(stream)
+            graph.search(int(s), out=out, stream=stream)
+            ends[k].record(stream)
+        barrier()
+        apsp.sparse_timing_enable(False)
+    search_ms, searches, kernels = apsp.sparse_timing_read()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps * m / (total_ms * 1e-3)
+
+    check = None
+    if rank == 0:
+        import oracle
+
+        last = int(src[-1])
+        check = bool(np.array_equal(out.cpu().numpy(), oracle.dijkstra_csr_i32(row_ptr, col, w, [last])[0]))
+
+    e2e = None
+    if not args.no_e2e:
+        # the graph goes to the device once (it is the input of every search);
+        # per step: the source index is the whole input, the distances come back
+        host_out = torch.empty(n, dtype=torch.int32).pin_memory()
+        times = []
+        for it, s in enumerate(src[:args.steps + 1]):
+            barrier()
+            t0 = time.perf_counter()
+            graph.search(int(s), out=out, stream=stream)
+            host_out.copy_(out, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+            if it > 0:
+                times.append(time.perf_counter() - t0)
+        e2e_total = sum(times)
+        e2e = {"value": world * args.steps * m / e2e_total, "unit": "TEPS", "h2d_bytes_per_step": 4,
+               "d2h_bytes_per_step": n * 4, "ms_per_step": e2e_total / args.steps * 1e3,
+               "graph_h2d_bytes_once": int(row_ptr.nbytes + col.nbytes + w.nbytes)}
+
+    clk = clocks.summary()
+    pk = peaks()
+    hbm = pk.get("hbm_gbs") or pk.get("hbm_GBps") or 6800.0
+    roof = None
+    if searches:
+        avg = search_ms / searches
+        algo_bytes = 8.0 * m + 16.0 * n
+        achieved = algo_bytes / (avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": "sssp_grid_kernel", "avg_launch_ms": avg, "launches": searches,
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "peak_basis": "MEASURED_PEAKS.json hbm_gbs" if pk.get("hbm_gbs") else "fallback 6.8 TB/s",
+                "search_share": search_ms / total_ms if total_ms > 0 else None}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        t0 = time.perf_counter()
+        oracle.dijkstra_csr_i32(row_ptr, col, w, [int(src[0])], threads=1)
+        dt = time.perf_counter() - t0
+        cpu = {"value": m / dt, "unit": "TEPS", "cores": 1, "kind": "oracle",
+               "sample": f"the oracle's binary-heap Dijkstra from one source ({dt:.1f} s, 1 thread)"}
+
+    if rank == 0:
+        line = {
+            "metric": SSSP_METRIC, "value": value, "unit": "TEPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": f"rmat{args.scale}", "n": n, "m": m, "graph": graphgen.describe_rmat(args.scale),
+                       "algo": "sssp", "delta": delta_used,
+                       "l2": f"graph {(row_ptr.nbytes + col.nbytes + w.nbytes) / 2**30:.2f} GiB resident; "
+                             "one seeded random source per step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": kernels, "clocks": clk, "check_vs_oracle": check, "step_ms": step_ms,
+        }
+        print(json.dumps(line), flush=True)
+    graph.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.algo == "sssp":
+        if args.impl == "reference":
+            reference_sssp(args, rank)
+        else:
+            ours_sssp(args, rank, world, local)
+        return
     if args.algo == "johnson":
         if args.impl == "reference":
             reference_johnson(args, rank)

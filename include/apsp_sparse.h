@@ -126,6 +126,32 @@ apsp_status_t apsp_sssp_i32(const int64_t* row_ptr, const int32_t* col_idx, cons
                             int32_t delta, int32_t* dist, apsp_stream_t stream);
 
 /*
+ * Prepared graphs for repeated single-source searches.  apsp_sssp_i32
+ * checks and partitions the arcs (light first, against delta) on every call;
+ * a prepared graph does that once, like building the CSR, and each search
+ * then runs on it alone.
+ *
+ * apsp_sssp_graph_create -- check the CSR graph (as apsp_sssp_i32), choose
+ *   delta (<= 0: the library's default), and build the graph's own device
+ *   copy: row_ptr, the partitioned arcs and the search state.  The caller's
+ *   arrays may be freed afterwards.  Blocks on `stream`.  *out receives the
+ *   handle (NULL on failure).  Status codes as for apsp_sssp_i32.
+ * apsp_sssp_graph_search -- one search from `source` into dist (device
+ *   int32[n], 16-byte aligned), on the device the graph was created on (else
+ *   APSP_EINVAL).  Blocks on `stream`.  Searches on one graph run one at a
+ *   time.
+ * apsp_sssp_graph_info -- n, m and the delta in use (any pointer may be NULL).
+ * apsp_sssp_graph_destroy -- free the graph (NULL is a no-op).
+ */
+typedef struct apsp_sssp_graph* apsp_sssp_graph_t;
+
+apsp_status_t apsp_sssp_graph_create(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
+                                     int32_t delta, apsp_stream_t stream, apsp_sssp_graph_t* out);
+apsp_status_t apsp_sssp_graph_search(apsp_sssp_graph_t graph, int source, int32_t* dist, apsp_stream_t stream);
+apsp_status_t apsp_sssp_graph_info(apsp_sssp_graph_t graph, int* n, long long* m, int32_t* delta);
+apsp_status_t apsp_sssp_graph_destroy(apsp_sssp_graph_t graph);
+
+/*
  * apsp_csr_count_i32 / apsp_csr_fill_i32 -- build the CSR of a dense int32
  * device matrix, with the arcs as defined above.
  * count: writes row_ptr (device, int64[n + 1]), and the arc count m to

@@ -102,6 +102,14 @@ def load():
         lib.apsp_sparse_release.restype = i32
         lib.apsp_sssp_i32.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         lib.apsp_sssp_i32.restype = i32
+        lib.apsp_sssp_graph_create.argtypes = [vp, vp, vp, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.apsp_sssp_graph_create.restype = i32
+        lib.apsp_sssp_graph_search.argtypes = [vp, i32, vp, vp]
+        lib.apsp_sssp_graph_search.restype = i32
+        lib.apsp_sssp_graph_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i32)]
+        lib.apsp_sssp_graph_info.restype = i32
+        lib.apsp_sssp_graph_destroy.argtypes = [vp]
+        lib.apsp_sssp_graph_destroy.restype = i32
         lib.apsp_sparse_timing_enable.argtypes = [i32]
         lib.apsp_sparse_timing_enable.restype = i32
         lib.apsp_sparse_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
@@ -376,6 +384,57 @@ def sssp(row_ptr, col_idx, w, source: int, delta: int = 0, out=None, stream=None
                                  w.data_ptr() if w.numel() else None, n, int(source), int(delta),
                                  out.data_ptr(), s), "apsp_sssp_i32")
     return out
+
+
+class SsspGraph:
+    """A CSR graph prepared once for repeated single-source searches
+    (apsp_sssp_graph_* in include/apsp_sparse.h).  The library keeps its own
+    device copy, so the tensors passed in may be dropped afterwards."""
+
+    def __init__(self, row_ptr, col_idx, w, delta: int = 0, stream=None):
+        import torch
+
+        lib = load()
+        n = _csr_args(row_ptr, col_idx, w)
+        self._dev = row_ptr.device
+        h = ctypes.c_void_p()
+        s = _stream_handle(row_ptr, stream)
+        with torch.cuda.device(self._dev):
+            _check(lib.apsp_sssp_graph_create(row_ptr.data_ptr(), col_idx.data_ptr() if col_idx.numel() else None,
+                                              w.data_ptr() if w.numel() else None, n, int(delta), s,
+                                              ctypes.byref(h)), "apsp_sssp_graph_create")
+        self._h = h
+
+    def info(self):
+        """(n, m, delta)."""
+        n, m, d = ctypes.c_int(), ctypes.c_longlong(), ctypes.c_int()
+        _check(load().apsp_sssp_graph_info(self._h, ctypes.byref(n), ctypes.byref(m), ctypes.byref(d)),
+               "apsp_sssp_graph_info")
+        return n.value, m.value, d.value
+
+    def search(self, source: int, out=None, stream=None):
+        import torch
+
+        n = self.info()[0]
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=self._dev)
+        if out.dtype != torch.int32 or out.dim() != 1 or out.numel() != n or not out.is_contiguous():
+            raise ValueError("out must be a contiguous int32 CUDA tensor of n entries")
+        s = _stream_handle(out, stream)
+        with torch.cuda.device(self._dev):
+            _check(load().apsp_sssp_graph_search(self._h, int(source), out.data_ptr(), s), "apsp_sssp_graph_search")
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(load().apsp_sssp_graph_destroy(self._h), "apsp_sssp_graph_destroy")
+        self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def sparse_release() -> None:

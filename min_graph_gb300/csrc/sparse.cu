@@ -34,6 +34,7 @@
 #include <climits>
 #include <cstdint>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "../../include/apsp.h"
@@ -207,15 +208,25 @@ __global__ void reweight_kernel(const int64_t* __restrict__ rp, const int32_t* _
 // Light-first partition of each vertex's arcs against delta, packed as
 // (head, weight) pairs: arcs[rp[u] .. rp[u] + nlight[u]) are the light arcs
 // (w <= delta) of u and the rest of its range the heavy ones, each part in
-// CSR order (warp per vertex, two ballot passes).
+// CSR order.  partition_kernel takes a warp per vertex (two ballot passes);
+// a vertex with more than kPartBig arcs is put on a list instead, for
+// partition_big_kernel, which gives each such vertex a whole CTA.
+constexpr int kPartBig = 8192;
+constexpr int kPartBigThreads = 1024;
+
 __global__ void partition_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
                                  const int32_t* __restrict__ w, int n, int32_t delta, int2* __restrict__ arcs,
-                                 int32_t* __restrict__ nlight) {
+                                 int32_t* __restrict__ nlight, int32_t* __restrict__ biglist,
+                                 int* __restrict__ bigcount) {
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= n) return;
     const int u = (int)wid;
     const int64_t beg = rp[u], end = rp[u + 1];
+    if (end - beg > kPartBig) {
+        if (lane == 0) biglist[atomicAdd(bigcount, 1)] = u;
+        return;
+    }
     int nl = 0;
     for (int64_t e = beg + lane; e < end; e += 32) nl += w[e] <= delta ? 1 : 0;
     nl = __reduce_add_sync(0xffffffffu, nl);
@@ -233,6 +244,56 @@ __global__ void partition_kernel(const int64_t* __restrict__ rp, const int32_t* 
         hpos += __popc(mh);
     }
     if (lane == 0) nlight[u] = nl;
+}
+
+// One CTA per listed vertex: the same stable light-first partition, the
+// arcs taken 1024 at a time with CTA-wide ranks (warp ballots plus a scan of
+// the 32 warps' counts).
+__global__ void __launch_bounds__(kPartBigThreads)
+partition_big_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ col,
+                     const int32_t* __restrict__ w, int32_t delta, int2* __restrict__ arcs,
+                     int32_t* __restrict__ nlight, const int32_t* __restrict__ biglist) {
+    __shared__ int s_light[32], s_heavy[32], s_total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = biglist[blockIdx.x];
+    const int64_t beg = rp[u], end = rp[u + 1];
+    int nl = 0;
+    for (int64_t e = beg + tid; e < end; e += kPartBigThreads) nl += w[e] <= delta ? 1 : 0;
+    nl = __reduce_add_sync(0xffffffffu, nl);
+    if (tid == 0) s_total = 0;
+    __syncthreads();
+    if (lane == 0) atomicAdd(&s_total, nl);
+    __syncthreads();
+    const int64_t light_total = s_total;
+    const unsigned lt = (1u << lane) - 1u;
+    int64_t lpos = beg, hpos = beg + light_total;  // the same in every thread
+    for (int64_t e0 = beg; e0 < end; e0 += kPartBigThreads) {
+        const int64_t e = e0 + tid;
+        const bool valid = e < end;
+        const int32_t c = valid ? col[e] : 0, ww = valid ? w[e] : 0;
+        const bool light = valid && ww <= delta, heavy = valid && ww > delta;
+        const unsigned ml = __ballot_sync(0xffffffffu, light), mh = __ballot_sync(0xffffffffu, heavy);
+        if (lane == 0) {
+            s_light[warp] = __popc(ml);
+            s_heavy[warp] = __popc(mh);
+        }
+        __syncthreads();
+        int lb = 0, hb = 0, lsum = 0, hsum = 0;
+        for (int x = 0; x < kPartBigThreads / 32; ++x) {
+            if (x < warp) {
+                lb += s_light[x];
+                hb += s_heavy[x];
+            }
+            lsum += s_light[x];
+            hsum += s_heavy[x];
+        }
+        if (light) arcs[lpos + lb + __popc(ml & lt)] = make_int2(c, ww);
+        if (heavy) arcs[hpos + hb + __popc(mh & lt)] = make_int2(c, ww);
+        lpos += lsum;
+        hpos += hsum;
+        __syncthreads();  // s_light / s_heavy are rewritten next
+    }
+    if (tid == 0) nlight[u] = (int32_t)light_total;
 }
 
 struct SpShared {
@@ -904,11 +965,13 @@ struct Work {
     int32_t* wh;
     int2* arcs;
     int32_t* nlight;
+    int32_t* biglist;  // vertices with more than kPartBig arcs
+    int* bigcount;
 };
 
 size_t work_bytes(int n, long long m) {
     const size_t mm = (size_t)(m > 0 ? m : 1);
-    return 256 + align256((size_t)n * 8) + align256(mm * 4) + align256(mm * 8) + align256((size_t)n * 4);
+    return 256 + align256((size_t)n * 8) + align256(mm * 4) + align256(mm * 8) + 2 * align256((size_t)n * 4);
 }
 
 Work work_layout(void* base, int n, long long m) {
@@ -927,6 +990,9 @@ Work work_layout(void* base, int n, long long m) {
     wk.arcs = reinterpret_cast<int2*>(b + off);
     off += align256(mm * 8);
     wk.nlight = reinterpret_cast<int32_t*>(b + off);
+    off += align256((size_t)n * 4);
+    wk.biglist = reinterpret_cast<int32_t*>(b + off);
+    wk.bigcount = wk.range + 7;
     return wk;
 }
 
@@ -984,6 +1050,28 @@ apsp_status_t check_row_ptr(const int64_t* rp, int n, int* flag, cudaStream_t s)
     return bad ? APSP_EINVAL : APSP_OK;
 }
 
+// The light-first partition of all arcs (partition_kernel, then
+// partition_big_kernel for the listed high-degree vertices).  Blocks on s.
+apsp_status_t partition_arcs(const int64_t* rp, const int32_t* col, const int32_t* w, int n, int32_t delta,
+                             int2* arcs, int32_t* nlight, int32_t* biglist, int* bigcount, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(bigcount, 0, sizeof(int), s);
+    if (e != cudaSuccess) return sp_fail(e);
+    partition_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, delta, arcs, nlight, biglist, bigcount);
+    count_kernel();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return sp_fail(e);
+    int big = 0;
+    apsp_status_t rc = read_int(bigcount, &big, s);
+    if (rc != APSP_OK) return rc;
+    if (big > 0) {
+        partition_big_kernel<<<big, kPartBigThreads, 0, s>>>(rp, col, w, delta, arcs, nlight, biglist);
+        count_kernel();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return sp_fail(e);
+    }
+    return APSP_OK;
+}
+
 // Bucket width when the caller gives none: 3 * w_max / (mean out-degree),
 // so that with weights spread over [0, w_max] a vertex has about three light
 // arcs.  The Delta-stepping page tunes Delta by measurement (section 4.4);
@@ -1014,10 +1102,10 @@ apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int3
 apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m,
                           const int32_t* sources, int nsrc, int32_t delta, const long long* h, int32_t* out,
                           long long ldo, const Work& wk, cudaStream_t s) {
-    partition_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, delta, wk.arcs, wk.nlight);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return sp_fail(e);
     (void)m;
+    apsp_status_t prc = partition_arcs(rp, col, w, n, delta, wk.arcs, wk.nlight, wk.biglist, wk.bigcount, s);
+    if (prc != APSP_OK) return prc;
+    cudaError_t e;
     const size_t smem = sssp_smem_bytes(n);
     e = cudaFuncSetAttribute(sssp_delta_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
@@ -1052,7 +1140,7 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
     }
     apsp_status_t rc = wide ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
                             : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
-    count_kernel(2);  // partition + search
+    count_kernel();  // the search
     if (rc == APSP_OK && ev[1]) {
         e = cudaEventRecord(ev[1], s);
         if (e != cudaSuccess) rc = sp_fail(e);
@@ -1151,20 +1239,30 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
     return APSP_OK;
 }
 
-// Grid-search buffer: [ctrl 256 B | flags 256 B | nlight | queued | wmin |
-// front | rset | arcs], each section 256-byte aligned.
-size_t grid_bytes(int n, long long m) {
+// Grid-search buffer: [ctrl 256 B | flags 256 B | (row_ptr copy) | nlight |
+// queued | wmin | front | rset | arcs | big-vertex list], each section
+// 256-byte aligned.  flags: [0..2] weight range, [4] row_ptr check, [6]
+// big-vertex count.
+size_t grid_bytes(int n, long long m, bool own_rp) {
     const size_t nw = (size_t)(n + 31) / 32;
-    return 512 + align256((size_t)n * 4) + 4 * align256(nw * 4) + align256((size_t)(m > 0 ? m : 1) * 8);
+    return 512 + (own_rp ? align256((size_t)(n + 1) * 8) : 0) + 2 * align256((size_t)n * 4) +
+           4 * align256(nw * 4) + align256((size_t)(m > 0 ? m : 1) * 8);
 }
 
-apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m, int src,
-                          int32_t delta, int32_t* dist, char* buf, cudaStream_t s) {
+// Check the graph, choose delta, lay out `buf` and partition the arcs into
+// it.  With own_rp the buffer also keeps a copy of row_ptr, so that the
+// caller's arrays are not needed afterwards.  Blocks on s.
+apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m, int32_t delta,
+                           char* buf, bool own_rp, GridArgs& a, cudaStream_t s) {
     const size_t nw = (size_t)(n + 31) / 32;
-    GridArgs a;
     a.ctrl = reinterpret_cast<GridCtrl*>(buf);
-    int* flags = reinterpret_cast<int*>(buf + 256);  // [0..2] weight range, [4] row_ptr check
+    int* flags = reinterpret_cast<int*>(buf + 256);
     size_t off = 512;
+    int64_t* rp_copy = nullptr;
+    if (own_rp) {
+        rp_copy = reinterpret_cast<int64_t*>(buf + off);
+        off += align256((size_t)(n + 1) * 8);
+    }
     int32_t* nlight = reinterpret_cast<int32_t*>(buf + off);
     off += align256((size_t)n * 4);
     a.queued = reinterpret_cast<uint32_t*>(buf + off);
@@ -1176,12 +1274,13 @@ apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* 
     a.rset = reinterpret_cast<uint32_t*>(buf + off);
     off += align256(nw * 4);
     int2* arcs = reinterpret_cast<int2*>(buf + off);
-    a.rp = rp;
+    off += align256((size_t)(m > 0 ? m : 1) * 8);
+    int32_t* biglist = reinterpret_cast<int32_t*>(buf + off);
     a.nlight = nlight;
     a.arcs = arcs;
     a.n = n;
     a.nw = (int)nw;
-    a.dist = dist;
+    a.dist = nullptr;
     a.timeout_ns = 2000000000ull;
 
     apsp_status_t rc = check_row_ptr(rp, n, flags + 4, s);
@@ -1192,7 +1291,18 @@ apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* 
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
     if (delta <= 0) delta = default_delta(n, m, hi);
     a.delta = delta;
+    if (own_rp) {
+        const cudaError_t e = cudaMemcpyAsync(rp_copy, rp, (size_t)(n + 1) * 8, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return sp_fail(e);
+        a.rp = rp_copy;
+    } else {
+        a.rp = rp;
+    }
+    return partition_arcs(rp, col, w, n, delta, arcs, nlight, biglist, flags + 6, s);
+}
 
+// CTAs of the cooperative search launch: 2 per SM (all resident at once).
+apsp_status_t grid_size(int* grid) {
     int dev = 0, sms = 0, coop = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1200,12 +1310,20 @@ apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* 
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_grid_kernel, kGridThreads, 0);
     if (e != cudaSuccess) return sp_fail(e);
     if (!coop || per_sm < 1) return APSP_EUNSUPPORTED;
-    const int grid = sms * min(per_sm, 2);
+    *grid = sms * min(per_sm, 2);
+    return APSP_OK;
+}
 
-    partition_kernel<<<blocks_for_warps(n), 256, 0, s>>>(rp, col, w, n, delta, arcs, nlight);
-    grid_init_kernel<<<sms * 4, 256, 0, s>>>(a, src);
-    count_kernel(2);
-    e = cudaGetLastError();
+// One search from src on a prepared graph into dist.  Blocks on s.
+apsp_status_t grid_run(const GridArgs& prepared, int src, int32_t* dist, cudaStream_t s) {
+    GridArgs a = prepared;
+    a.dist = dist;
+    int grid = 0;
+    apsp_status_t rc = grid_size(&grid);
+    if (rc != APSP_OK) return rc;
+    grid_init_kernel<<<grid * 2, 256, 0, s>>>(a, src);
+    count_kernel();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return sp_fail(e);
     cudaEvent_t ev[2] = {nullptr, nullptr};
     if (g_sp_timing.enabled) {
@@ -1223,7 +1341,7 @@ apsp_status_t grid_search(const int64_t* rp, const int32_t* col, const int32_t* 
     count_kernel();
     if (e == cudaSuccess && ev[1]) e = cudaEventRecord(ev[1], s);
     if (e == cudaSuccess) {
-        grid_finish_kernel<<<sms * 4, 256, 0, s>>>(dist, n);
+        grid_finish_kernel<<<grid * 2, 256, 0, s>>>(dist, a.n);
         count_kernel();
         e = cudaGetLastError();
     }
@@ -1263,11 +1381,88 @@ apsp_status_t apsp_sssp_i32(const int64_t* row_ptr, const int32_t* col_idx, cons
     apsp_status_t rc = read_m(row_ptr, n, &m, s);
     if (rc != APSP_OK) return rc;
     if (m < 0 || m >= (long long)INT_MAX || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
-    rc = grow(st->grid, grid_bytes(n, m));
+    rc = grow(st->grid, grid_bytes(n, m, false));
     if (rc != APSP_OK) return rc;
-    return grid_search(row_ptr, col_idx, w, n, m, source, delta, dist, static_cast<char*>(st->grid.p), s);
+    GridArgs a;
+    rc = grid_prepare(row_ptr, col_idx, w, n, m, delta, static_cast<char*>(st->grid.p), false, a, s);
+    if (rc != APSP_OK) return rc;
+    return grid_run(a, source, dist, s);
 }
 
+}  // extern "C"
+
+struct apsp_sssp_graph {
+    int device = 0;
+    long long m = 0;
+    void* buf = nullptr;
+    GridArgs a;
+};
+
+extern "C" {
+
+apsp_status_t apsp_sssp_graph_create(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
+                                     int32_t delta, apsp_stream_t stream, apsp_sssp_graph_t* out) {
+    if (out == nullptr) return APSP_EINVAL;
+    *out = nullptr;
+    if (n <= 0 || row_ptr == nullptr) return APSP_EINVAL;
+    if (!sp_supported_device()) return APSP_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    long long m = 0;
+    apsp_status_t rc = read_m(row_ptr, n, &m, s);
+    if (rc != APSP_OK) return rc;
+    if (m < 0 || m >= (long long)INT_MAX || (m > 0 && (col_idx == nullptr || w == nullptr))) return APSP_EINVAL;
+    apsp_sssp_graph* g = new (std::nothrow) apsp_sssp_graph;
+    if (!g) return APSP_ENOMEM;
+    cudaGetDevice(&g->device);
+    g->m = m;
+    const cudaError_t e = cudaMalloc(&g->buf, grid_bytes(n, m, true));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        apsp::set_last_cuda_error((int)e);
+        delete g;
+        return APSP_ENOMEM;
+    }
+    rc = grid_prepare(row_ptr, col_idx, w, n, m, delta, static_cast<char*>(g->buf), true, g->a, s);
+    if (rc != APSP_OK) {
+        cudaStreamSynchronize(s);
+        cudaFree(g->buf);
+        delete g;
+        return rc;
+    }
+    *out = g;
+    return APSP_OK;
+}
+
+apsp_status_t apsp_sssp_graph_search(apsp_sssp_graph_t g, int source, int32_t* dist, apsp_stream_t stream) {
+    if (g == nullptr || dist == nullptr || source < 0 || source >= g->a.n) return APSP_EINVAL;
+    if (reinterpret_cast<uintptr_t>(dist) % 16 != 0) return APSP_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != g->device) return APSP_EINVAL;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    return grid_run(g->a, source, dist, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_sssp_graph_info(apsp_sssp_graph_t g, int* n, long long* m, int32_t* delta) {
+    if (g == nullptr) return APSP_EINVAL;
+    if (n) *n = g->a.n;
+    if (m) *m = g->m;
+    if (delta) *delta = g->a.delta;
+    return APSP_OK;
+}
+
+apsp_status_t apsp_sssp_graph_destroy(apsp_sssp_graph_t g) {
+    if (g == nullptr) return APSP_OK;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != g->device) cudaSetDevice(g->device);
+    cudaDeviceSynchronize();
+    cudaFree(g->buf);
+    if (cur != g->device) cudaSetDevice(cur);
+    delete g;
+    return APSP_OK;
+}
 
 apsp_status_t apsp_csr_count_i32(const int32_t* dist, int n, int ld, int64_t* row_ptr, long long* m_out,
                                  apsp_stream_t stream) {

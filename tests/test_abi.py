@@ -99,6 +99,14 @@ def test_sparse_bad_arguments_rejected_without_cuda(libs):
     assert lib.apsp_sssp_i32(fake, fake, fake, 5, -1, 0, fake, None) == apsp.EINVAL   # source < 0
     assert lib.apsp_sssp_i32(fake, fake, fake, 5, 0, 0, None, None) == apsp.EINVAL    # no output
     assert lib.apsp_sssp_i32(fake, fake, fake, 5, 0, 0, ctypes.c_void_p(0x1004), None) == apsp.EINVAL  # misaligned
+    h = ctypes.c_void_p(0x1234)
+    assert lib.apsp_sssp_graph_create(fake, fake, fake, 5, 0, None, None) == apsp.EINVAL   # no handle slot
+    assert lib.apsp_sssp_graph_create(None, fake, fake, 5, 0, None, ctypes.byref(h)) == apsp.EINVAL
+    assert h.value is None                                                             # cleared on failure
+    assert lib.apsp_sssp_graph_create(fake, fake, fake, 0, 0, None, ctypes.byref(h)) == apsp.EINVAL
+    assert lib.apsp_sssp_graph_search(None, 0, fake, None) == apsp.EINVAL
+    assert lib.apsp_sssp_graph_info(None, None, None, None) == apsp.EINVAL
+    assert lib.apsp_sssp_graph_destroy(None) == apsp.OK
 
 
 def test_python_binding_rejects_non_cuda():

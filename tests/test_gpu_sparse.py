@@ -50,6 +50,10 @@ def csr_of(w: np.ndarray):
     return np.cumsum(row_ptr), cols.astype(np.int32), w[rows, cols].astype(np.int32)
 
 
+def dev(*arrays):
+    return [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in arrays]
+
+
 def to_dev(*arrays):
     return [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in arrays]
 
@@ -292,3 +296,13 @@ def test_l2_probe_reports_a_bandwidth():
 
     r = peak.l2_read(8 << 20, passes=4)
     assert r["gbs"] > 100.0
+
+
+def test_dense_rows_take_the_cta_partition():
+    # 9000 vertices with ~8500 arcs each: rows above 8192 arcs are partitioned
+    # one CTA per vertex; four searches against Dijkstra rows
+    w = graphgen.er_i32(9000, 0.95, 1, 1000, seed=40)
+    rp, col, wt = dev(*csr_of(w))
+    src = np.array([0, 1, 4500, 8999], dtype=np.int32)
+    got = apsp.sssp_delta(rp, col, wt, torch.from_numpy(src).cuda())
+    assert_i32_exact(got.cpu().numpy(), oracle.dijkstra_i32(w, src), "dense rows")

@@ -136,3 +136,40 @@ def test_bad_inputs_rejected():
 def test_rmat_scale20_sampled_sources():
     row_ptr, col, w = graphgen.rmat_csr(20)
     check(row_ptr, col, w, [0, 123457], what="rmat20")
+
+
+def test_prepared_graph_searches():
+    row_ptr, col, w = graphgen.rmat_csr(15, whi=3000, seed=5)
+    g = dev(row_ptr, col, w)
+    graph = apsp.SsspGraph(*g)
+    n, m, delta = graph.info()
+    assert n == 1 << 15 and m == int(row_ptr[-1]) and delta > 0
+    del g  # the prepared graph keeps its own copy
+    torch.cuda.empty_cache()
+    src = [0, 7, 32767, 12345]
+    ref = oracle.dijkstra_csr_i32(row_ptr, col, w, src)
+    out = torch.empty(n, dtype=torch.int32, device="cuda")
+    for q, s_ in enumerate(src):
+        assert_i32_exact(graph.search(s_, out=out).cpu().numpy(), ref[q], f"prepared source {s_}")
+    with pytest.raises(apsp.ApspError) as ei:
+        graph.search(n)
+    assert ei.value.status == apsp.EINVAL
+    graph.close()
+    graph.close()  # idempotent
+    bad = dev(row_ptr, col, -w)
+    with pytest.raises(apsp.ApspError) as ei:
+        apsp.SsspGraph(*bad)
+    assert ei.value.status == apsp.EINVAL
+
+
+def test_partition_of_a_hub_larger_than_a_warp_pass():
+    # a vertex with 300000 arcs takes the one-CTA-per-vertex partition
+    rng = np.random.default_rng(8)
+    n = 50000
+    tail = np.concatenate([rng.integers(0, n, 100000), np.full(300000, 4)])
+    head = rng.integers(0, n, tail.size)
+    wt = rng.integers(0, 5000, tail.size).astype(np.int32)
+    order = np.argsort(tail, kind="stable")
+    row_ptr = np.concatenate([[0], np.cumsum(np.bincount(tail, minlength=n))]).astype(np.int64)
+    for delta in (0, 1, 2500):
+        check(row_ptr, head[order].astype(np.int32), wt[order], [4, 9], delta=delta, what="mega hub")
