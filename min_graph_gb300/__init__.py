@@ -110,6 +110,13 @@ def load():
         lib.apsp_sssp_graph_info.restype = i32
         lib.apsp_sssp_graph_destroy.argtypes = [vp]
         lib.apsp_sssp_graph_destroy.restype = i32
+        u64 = ctypes.c_ulonglong
+        for name in ("apsp_solve_ooc_i32", "apsp_solve_ooc_f32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, i32, i32, u64, i32, vp]
+            f.restype = i32
+        lib.apsp_ooc_block.argtypes = [i32, u64, i32]
+        lib.apsp_ooc_block.restype = i32
         lib.apsp_sparse_timing_enable.argtypes = [i32]
         lib.apsp_sparse_timing_enable.restype = i32
         lib.apsp_sparse_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
@@ -205,6 +212,41 @@ def solve_host(a, n: int | None = None, ld: int | None = None, stream=None):
     else:
         raise TypeError("dtype must be int32 or float32")
     return a
+
+
+def solve_ooc(a, device_bytes: int = 0, block: int = 0, stream=None):
+    """Out-of-core APSP on a HOST matrix (numpy array or CPU tensor; pin it
+    for overlapped copies), streamed through the GPU in K x K super-blocks
+    (include/apsp_ooc.h).  device_bytes caps the device memory used (0: 70%
+    of what is free); block is K (0: the largest that fits).  In place,
+    blocking.  Returns a."""
+    import numpy as np
+    import torch
+
+    lib = load()
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or a.dim() != 2 or a.shape[0] != a.shape[1] or (a.shape[0] > 1 and a.stride(1) != 1):
+            raise ValueError("expected a square row-major CPU tensor")
+        ptr, n, ld = a.data_ptr(), a.shape[0], a.stride(0)
+        is_i32, is_f32 = a.dtype == torch.int32, a.dtype == torch.float32
+    else:
+        if not isinstance(a, np.ndarray) or a.ndim != 2 or a.shape[0] != a.shape[1] or not a.flags.c_contiguous:
+            raise ValueError("expected a square C-contiguous numpy array")
+        ptr, n, ld = a.ctypes.data, a.shape[0], a.shape[1]
+        is_i32, is_f32 = a.dtype == np.int32, a.dtype == np.float32
+    s = 0 if stream is None else (int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+    if is_i32:
+        _check(lib.apsp_solve_ooc_i32(ptr, n, max(ld, 1), int(device_bytes), int(block), s), "apsp_solve_ooc_i32")
+    elif is_f32:
+        _check(lib.apsp_solve_ooc_f32(ptr, n, max(ld, 1), int(device_bytes), int(block), s), "apsp_solve_ooc_f32")
+    else:
+        raise TypeError("dtype must be int32 or float32")
+    return a
+
+
+def ooc_block(n: int, device_bytes: int, elem_bytes: int = 4) -> int:
+    """The super-block K that solve_ooc would choose (0: nothing fits)."""
+    return load().apsp_ooc_block(int(n), int(device_bytes), int(elem_bytes))
 
 
 def validate(t, stream=None) -> int:

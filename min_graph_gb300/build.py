@@ -21,7 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 
 LIBS = {
-    "libapsp.so": ["apsp_api.cu", "fw_i32.cu", "fw_f32.cu", "noalloc.cu", "sparse.cu"],
+    "libapsp.so": ["apsp_api.cu", "fw_i32.cu", "fw_f32.cu", "noalloc.cu", "sparse.cu", "ooc.cu"],
     "libapsp_peak.so": ["peak.cu"],
 }
 HEADERS = ["fw_kernels.cuh", "fw_fused.cuh", "fw_launch.h", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"]

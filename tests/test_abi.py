@@ -25,7 +25,7 @@ def declared_functions(header: str):
 
 
 @pytest.mark.parametrize("header,lib", [("apsp.h", "libapsp.so"), ("apsp_debug.h", "libapsp.so"),
-                                        ("apsp_sparse.h", "libapsp.so"),
+                                        ("apsp_sparse.h", "libapsp.so"), ("apsp_ooc.h", "libapsp.so"),
                                         ("apsp_peak.h", "libapsp_peak.so")])
 def test_every_declared_symbol_is_exported(libs, header, lib):
     names = declared_functions(header)
@@ -130,3 +130,25 @@ def test_workspace_layout_is_16_byte_aligned():
     for n in (1, 127, 128, 129, 1000, 32768):
         npad = -(-n // apsp.TILE) * apsp.TILE
         assert (apsp.TILE * npad * 4) % 65536 == 0
+
+
+def test_ooc_arguments_and_block_choice(libs):
+    lib = apsp.load()
+    fake = ctypes.c_void_p(0x1000)
+    for fn in (lib.apsp_solve_ooc_i32, lib.apsp_solve_ooc_f32):
+        assert fn(None, 5, 5, 1 << 30, 0, None) == apsp.EINVAL   # NULL with n > 0
+        assert fn(fake, 6, 5, 1 << 30, 0, None) == apsp.EINVAL   # ld < n
+        assert fn(fake, 5, 5, 1 << 30, 100, None) == apsp.EINVAL  # K not a multiple of 128
+        assert fn(fake, 5, 5, 1 << 30, -128, None) == apsp.EINVAL
+        assert fn(None, 0, 0, 0, 0, None) == apsp.OK
+    # 5 K^2 + 2 K npad elements of 4 bytes must fit the budget
+    def need(n, k):
+        npad = -(-n // k) * k
+        return 4 * (5 * k * k + 2 * k * npad)
+    for n, budget in ((1000, 1 << 20), (32768, 1 << 30), (100000, 8 << 30), (300, 1 << 30)):
+        k = apsp.ooc_block(n, budget)
+        assert k == 0 or (k % 128 == 0 and need(n, k) <= budget), (n, budget, k)
+        if k and k < min(16384, -(-n // 128) * 128):
+            assert need(n, k + 128) > budget, (n, budget, k)
+    assert apsp.ooc_block(300, 1 << 30) == 384          # the whole matrix is one super-block
+    assert apsp.ooc_block(100000, 1000) == 0            # not even K = 128 fits
