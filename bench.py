@@ -33,6 +33,12 @@ seeded random source, and the metric is traversed edges per second (m /
 search time).  Its roofline is HBM: 8 bytes per arc and 16 per vertex per
 search against the measured copy bandwidth.  The CPU baseline and the
 reference arm time the oracle's CSR Dijkstra from one source.
+
+--algo ooc measures the out-of-core solver (min_graph_gb300.solve_ooc): the
+workload's matrix in pinned host memory, streamed through the GPU in K x K
+super-blocks (--block).  A step is one whole blocking call, copies included,
+so value and e2e are the same figure; the input is restored on the host
+before each step, outside the timed region.
 """
 from __future__ import annotations
 
@@ -68,7 +74,9 @@ def parse():
     ap.add_argument("--workload", default="ba16384", choices=sorted(graphgen.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--algo", choices=["fw", "johnson", "sssp"], default="fw")
+    ap.add_argument("--algo", choices=["fw", "johnson", "sssp", "ooc"], default="fw")
+    ap.add_argument("--block", type=int, default=4096, help="super-block K for --algo ooc (0: from the budget)")
+    ap.add_argument("--device-bytes", type=int, default=0, help="device budget for --algo ooc (0: 70%% of free)")
     ap.add_argument("--scale", type=int, default=22, help="R-MAT scale for --algo sssp")
     ap.add_argument("--delta", type=int, default=0, help="Delta for --algo johnson (0: the library's default)")
     return ap.parse_args()
@@ -783,9 +791,91 @@ def ours_sssp(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ out-of-core arm
+
+def ours_ooc(args, rank, world, local):
+    import torch
+
+    import min_graph_gb300 as apsp
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = graphgen.make(args.workload)
+    n = w.shape[0]
+    src = torch.from_numpy(w)
+    host = torch.empty_like(src).pin_memory()
+    K = args.block or apsp.ooc_block(n, args.device_bytes or 0)
+    for _ in range(args.warmup):
+        host.copy_(src)
+        apsp.solve_ooc(host, device_bytes=args.device_bytes, block=args.block)
+    times = []
+    with ClockSampler(local) as clocks:
+        for _ in range(args.steps):
+            host.copy_(src)  # restore the input (outside the timed region)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            apsp.solve_ooc(host, device_bytes=args.device_bytes, block=args.block)
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * float(n) ** 3 / total
+    check = None
+    if rank == 0:
+        import oracle
+
+        rows = np.array([0, n // 3, (2 * n) // 3, n - 1], dtype=np.int32)
+        got = host.numpy()[rows]
+        if w.dtype == np.int32:
+            check = bool(np.array_equal(got, oracle.dijkstra_i32(w, rows)))
+        else:
+            ref = oracle.dijkstra_f32(w, rows)
+            fin = np.isfinite(ref)
+            check = bool(np.array_equal(np.isfinite(got), fin) and
+                         np.all(np.abs(got[fin] - ref[fin]) <= 1e-5 * np.abs(ref[fin])))
+    props = torch.cuda.get_device_properties(dev)
+    clk = clocks.summary()
+    f_max = (clk or {}).get("sm_max_mhz") or peaks().get("sm_max_mhz", 2070.0)
+    ops = 1 if w.dtype == np.int32 else 2
+    peak_tops = props.multi_processor_count * NOMINAL_INT32_LANES * f_max * 1e6 / ops / 1e12
+    nR = -(-n // K) if K else None
+    nbytes = n * n * w.itemsize
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and w.dtype == np.int32:
+        v, ksteps, secs, thr = cpu_oracle_sample(w)
+        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"first {ksteps} k-steps of the untiled Floyd-Warshall triple loop on the "
+                         f"full n={n} matrix ({secs:.1f} s, {thr} threads)"}
+    line = {
+        "metric": METRIC.replace(", 1 GPU", ", out-of-core from host memory, 1 GPU"), "value": value, "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32" if w.dtype == np.int32 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload), "algo": "ooc",
+                   "block": K, "super_rounds": nR, "host": "pinned; restored before each step, outside the timing",
+                   "parallelism": "1 GPU"},
+        "roofline": {"bound": "alu", "achieved": value / 1e12, "peak": peak_tops, "unit": "Trelax/s",
+                     "frac": value / 1e12 / peak_tops, "traffic": None, "kernel": "whole call (minplus_accum_kernel "
+                     "and the in-core solver, copies overlapped)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": int(nbytes * (nR or 1)),
+                "d2h_bytes_per_step": int(nbytes * (nR or 1)),
+                "note": "the call itself is end to end: about one crossing of the matrix each way per super-round"},
+        "clocks": clk, "check_rows_vs_oracle": check, "step_s": times,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.algo == "ooc":
+        if args.impl == "reference":
+            reference_arm(args, rank)
+        else:
+            ours_ooc(args, rank, world, local)
+        return
     if args.algo == "sssp":
         if args.impl == "reference":
             reference_sssp(args, rank)
