@@ -28,6 +28,19 @@ extern "C" {
  */
 apsp_status_t apsp_debug_inject_phase3_timeout(unsigned long long timeout_ns);
 
+/*
+ * apsp_debug_inject_grid_timeout -- arm a one-shot fault for the next
+ * grid-wide search (apsp_sssp_i32 or apsp_sssp_graph_search): CTA 0 leaves
+ * the cooperative launch before it reaches the first grid barrier.  The other
+ * CTAs' bounded waits at that barrier run out after `timeout_ns`; they record
+ * the timeout and leave, and the call returns APSP_ETIMEOUT.  dist is then
+ * undefined.  No fault, trap or unbounded wait is involved, and the next
+ * search on the same context is unaffected.
+ *   timeout_ns  1 .. 2e9 nanoseconds.
+ * Returns APSP_EINVAL for an out-of-range timeout.
+ */
+apsp_status_t apsp_debug_inject_grid_timeout(unsigned long long timeout_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,6 +88,8 @@ def load():
         lib.apsp_phase_timing_read.restype = i32
         lib.apsp_debug_inject_phase3_timeout.argtypes = [ctypes.c_ulonglong]
         lib.apsp_debug_inject_phase3_timeout.restype = i32
+        lib.apsp_debug_inject_grid_timeout.argtypes = [ctypes.c_ulonglong]
+        lib.apsp_debug_inject_grid_timeout.restype = i32
         lib.apsp_solve_sparse_i32.argtypes = [vp, i32, i32, i32, vp]
         lib.apsp_solve_sparse_i32.restype = i32
         lib.apsp_johnson_csr_i32.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
@@ -494,3 +496,10 @@ def sparse_timing_read():
     _check(load().apsp_sparse_timing_read(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(k)),
            "apsp_sparse_timing_read")
     return ms.value, n.value, k.value
+
+
+def debug_inject_grid_timeout(timeout_ns: int) -> None:
+    """Test hook (include/apsp_debug.h): the next grid-wide search loses CTA 0
+    before its first grid barrier, so the other CTAs' bounded waits run out
+    after `timeout_ns` and the call raises ApspError(ETIMEOUT)."""
+    _check(load().apsp_debug_inject_grid_timeout(int(timeout_ns)), "apsp_debug_inject_grid_timeout")

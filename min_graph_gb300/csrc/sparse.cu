@@ -38,6 +38,7 @@
 #include <vector>
 
 #include "../../include/apsp.h"
+#include "../../include/apsp_debug.h"
 #include "../../include/apsp_sparse.h"
 #include "tma.cuh"
 
@@ -579,6 +580,7 @@ struct GridArgs {
     uint32_t* rset;
     GridCtrl* ctrl;
     unsigned long long timeout_ns;
+    int inject;  // test hook: CTA 0 leaves before the first barrier
 };
 
 __device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
@@ -789,6 +791,7 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
 }
 
 __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) {
+    if (a.inject && blockIdx.x == 0) return;  // test hook (apsp_debug_inject_grid_timeout)
     __shared__ GridBig big;
     if (threadIdx.x == 0) big.count = 0;
     __syncthreads();
@@ -1282,6 +1285,7 @@ apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t*
     a.nw = (int)nw;
     a.dist = nullptr;
     a.timeout_ns = 2000000000ull;
+    a.inject = 0;
 
     apsp_status_t rc = check_row_ptr(rp, n, flags + 4, s);
     if (rc != APSP_OK) return rc;
@@ -1314,10 +1318,19 @@ apsp_status_t grid_size(int* grid) {
     return APSP_OK;
 }
 
+// Test hook state (apsp_debug_inject_grid_timeout), under g_sp_mu.
+bool g_grid_inject = false;
+unsigned long long g_grid_inject_ns = 0;
+
 // One search from src on a prepared graph into dist.  Blocks on s.
 apsp_status_t grid_run(const GridArgs& prepared, int src, int32_t* dist, cudaStream_t s) {
     GridArgs a = prepared;
     a.dist = dist;
+    if (g_grid_inject) {
+        a.inject = 1;
+        a.timeout_ns = g_grid_inject_ns;
+        g_grid_inject = false;
+    }
     int grid = 0;
     apsp_status_t rc = grid_size(&grid);
     if (rc != APSP_OK) return rc;
@@ -1575,6 +1588,14 @@ apsp_status_t apsp_solve_sparse_i32(int32_t* dist, int n, int ld, int32_t delta,
     const int32_t* w = reinterpret_cast<const int32_t*>(static_cast<const char*>(st->body.p) + colb);
     // The searches read only the CSR, so they may overwrite dist as they go.
     return johnson(rp, col, w, n, m, delta, dist, ld, work_layout(st->work.p, n, m), false, s);
+}
+
+apsp_status_t apsp_debug_inject_grid_timeout(unsigned long long timeout_ns) {
+    if (timeout_ns == 0 || timeout_ns > 2000000000ull) return APSP_EINVAL;
+    std::lock_guard<std::mutex> lock(g_sp_mu);
+    g_grid_inject = true;
+    g_grid_inject_ns = timeout_ns;
+    return APSP_OK;
 }
 
 apsp_status_t apsp_sparse_timing_enable(int enable) {

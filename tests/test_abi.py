@@ -71,6 +71,8 @@ def test_bad_arguments_rejected_without_cuda(libs):
     assert lib.apsp_phase_timing_enable(0) == apsp.OK
     assert lib.apsp_debug_inject_phase3_timeout(0) == apsp.EINVAL
     assert lib.apsp_debug_inject_phase3_timeout(3 * 10**9) == apsp.EINVAL
+    assert lib.apsp_debug_inject_grid_timeout(0) == apsp.EINVAL
+    assert lib.apsp_debug_inject_grid_timeout(3 * 10**9) == apsp.EINVAL
 
 
 def test_sparse_bad_arguments_rejected_without_cuda(libs):

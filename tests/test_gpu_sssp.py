@@ -173,3 +173,21 @@ def test_partition_of_a_hub_larger_than_a_warp_pass():
     row_ptr = np.concatenate([[0], np.cumsum(np.bincount(tail, minlength=n))]).astype(np.int64)
     for delta in (0, 1, 2500):
         check(row_ptr, head[order].astype(np.int32), wt[order], [4, 9], delta=delta, what="mega hub")
+
+
+def test_grid_barrier_timeout_is_reported_and_the_context_survives():
+    row_ptr, col, w = graphgen.rmat_csr(12, whi=1000, seed=2)
+    g = dev(row_ptr, col, w)
+    apsp.debug_inject_grid_timeout(50_000_000)  # 50 ms
+    with pytest.raises(apsp.ApspError) as ei:
+        apsp.sssp(*g, 0)
+    assert ei.value.status == apsp.ETIMEOUT
+    check(row_ptr, col, w, [0, 9], what="after a timeout")
+    graph = apsp.SsspGraph(*g)
+    apsp.debug_inject_grid_timeout(50_000_000)
+    with pytest.raises(apsp.ApspError) as ei:
+        graph.search(0)
+    assert ei.value.status == apsp.ETIMEOUT
+    ref = oracle.dijkstra_csr_i32(row_ptr, col, w, [0])[0]
+    assert_i32_exact(graph.search(0).cpu().numpy(), ref, "prepared, after a timeout")
+    graph.close()
