@@ -382,10 +382,12 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
 
         T acc[8][8];
         load_tile(acc, cbuf, L);
+        if (r <= 0) {  // from launch 1 on, every tile read was stored (clamped) by an earlier round
 #pragma unroll
-        for (int ri = 0; ri < 8; ++ri)
+            for (int ri = 0; ri < 8; ++ri)
 #pragma unroll
-            for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
+                for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
+        }
 
         if (w.kind == kItemP3) {
             // ------------------------------------------------ phase 3 (round r)
