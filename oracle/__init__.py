@@ -89,6 +89,8 @@ def bind(path: str):
     lib.oracle_bellman_ford_i32.restype = i32
     lib.oracle_johnson_i32.argtypes = [vp, i64, i64, vp, i32]
     lib.oracle_johnson_i32.restype = i32
+    lib.oracle_johnson_rows_i32.argtypes = [vp, i64, i64, vp, i64, vp, i32]
+    lib.oracle_johnson_rows_i32.restype = i32
     lib.oracle_dijkstra_csr_i32.argtypes = [vp, vp, vp, i64, vp, i64, vp, i32]
     lib.oracle_dijkstra_csr_i32.restype = i32
     return lib
@@ -218,6 +220,21 @@ class Oracle:
                                                 threads or default_threads()), "dijkstra_csr_i32")
         return out
 
+    def johnson_rows_i32(self, w: np.ndarray, sources, threads: int | None = None):
+        """Rows of Johnson's all-pairs distances for the given sources only
+        (the potentials still come from Bellman-Ford over the whole graph);
+        None on a negative cycle."""
+        w = _as_matrix(w, np.int32)
+        n = w.shape[0]
+        src = np.ascontiguousarray(np.asarray(sources, dtype=np.int32))
+        out = np.empty((src.size, n), dtype=np.int32)
+        rc = self.lib.oracle_johnson_rows_i32(w.ctypes.data, n, w.shape[1], src.ctypes.data, src.size,
+                                              out.ctypes.data, threads or default_threads())
+        if rc == 1:
+            return None
+        _check(rc, "johnson_rows_i32")
+        return out
+
     def bfs_hops_i32(self, w: np.ndarray, src: int) -> np.ndarray:
         w = _as_matrix(w, np.int32)
         hops = np.empty(w.shape[0], dtype=np.int32)
@@ -266,3 +283,7 @@ def johnson_i32(w, threads=None):
 
 def dijkstra_csr_i32(row_ptr, col, w, sources, threads=None):
     return default().dijkstra_csr_i32(row_ptr, col, w, sources, threads=threads)
+
+
+def johnson_rows_i32(w, sources, threads=None):
+    return default().johnson_rows_i32(w, sources, threads=threads)

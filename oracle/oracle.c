@@ -360,11 +360,16 @@ int oracle_bellman_ford_i32(const int32_t* w, int64_t n, int64_t ld, int64_t src
     return 0;
 }
 
-/* All-pairs distances by Johnson's method.  out is n x n (int32, INF for
- * unreachable).  Returns 0, 1 on a negative cycle, < 0 on bad arguments or
- * allocation failure. */
-int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, int threads) {
+/* Johnson's method for the rows of the sources (all rows when sources is
+ * NULL).  Row s of out (ns x n, int32, INF for unreachable) holds the
+ * distances from sources[s].  Returns 0, 1 on a negative cycle, < 0 on bad
+ * arguments or allocation failure. */
+static int o_johnson(const int32_t* w, int64_t n, int64_t ld, const int32_t* sources, int64_t ns, int32_t* out,
+                     int threads) {
     if (n <= 0 || ld < n || !w || !out) return -1;
+    if (!sources) ns = n;
+    for (int64_t s = 0; sources && s < ns; ++s)
+        if (sources[s] < 0 || sources[s] >= n) return -1;
     /* extendGraph + BellmanFord(s): s reaches every v directly with weight 0. */
     int64_t* h = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
     if (!h) return -2;
@@ -403,16 +408,17 @@ int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, in
             err = -2;
         } else {
 #pragma omp for schedule(dynamic, 1)
-            for (int64_t i = 0; i < n; ++i) {
+            for (int64_t q = 0; q < ns; ++q) {
+                const int64_t i = sources ? sources[q] : q;
                 if (o_dijkstra_one(&g, i, 1, di, df, st)) {  /* D(i) on w' */
 #pragma omp atomic write
                     err = -2;
                     continue;
                 }
                 for (int64_t j = 0; j < n; ++j) {            /* to(): D(i,j) = D'(i,j) + h(j) - h(i) */
-                    if (di[j] == INT64_MAX) { out[i * n + j] = (int32_t)O_INF; continue; }
+                    if (di[j] == INT64_MAX) { out[q * n + j] = (int32_t)O_INF; continue; }
                     const int64_t d = di[j] + h[j] - h[i];
-                    out[i * n + j] = (int32_t)(d < O_INF ? d : O_INF);
+                    out[q * n + j] = (int32_t)(d < O_INF ? d : O_INF);
                 }
             }
         }
@@ -421,6 +427,20 @@ int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, in
     o_graph_free(&g);
     free(h);
     return err;
+}
+
+/* All-pairs distances by Johnson's method.  out is n x n (int32, INF for
+ * unreachable).  Returns 0, 1 on a negative cycle, < 0 on bad arguments or
+ * allocation failure. */
+int oracle_johnson_i32(const int32_t* w, int64_t n, int64_t ld, int32_t* out, int threads) {
+    return o_johnson(w, n, ld, NULL, n, out, threads);
+}
+
+/* The same for the rows of the ns given sources only (out is ns x n). */
+int oracle_johnson_rows_i32(const int32_t* w, int64_t n, int64_t ld, const int32_t* sources, int64_t ns,
+                            int32_t* out, int threads) {
+    if (!sources || ns < 0) return -1;
+    return o_johnson(w, n, ld, sources, ns, out, threads);
 }
 
 /* ---------------- Dijkstra on a CSR graph ----------------

@@ -374,8 +374,29 @@ def check_dijkstra_csr(orc) -> list[str]:
     return bad
 
 
+def check_johnson_rows(orc) -> list[str]:
+    """Johnson's rows for chosen sources equal those rows of the full Johnson
+    matrix, and of the Floyd-Warshall matrix, on negative-weight graphs."""
+    bad = []
+    for seed in range(6):
+        n = 30 + 25 * seed
+        w = graphgen.er_potential_i32(n, 0.15, 0, 200, 150, seed=700 + seed)
+        src = np.random.default_rng(seed).choice(n, 5, replace=False)
+        rows = orc.johnson_rows_i32(w, src)
+        full = orc.johnson_i32(w)
+        if rows is None or full is None or not np.array_equal(rows, full[src]):
+            bad.append(f"johnson rows seed {seed}: differ from the full matrix")
+        elif not np.array_equal(rows, orc.fw_i32(w)[src]):
+            bad.append(f"johnson rows seed {seed}: differ from Floyd-Warshall")
+    w = graphgen.er_potential_i32(40, 0.2, 0, 50, 40, seed=9)
+    w[3, 7], w[7, 3] = -60, 10
+    if orc.johnson_rows_i32(w, [0, 1]) is not None:
+        bad.append("johnson rows: negative cycle not reported")
+    return bad
+
+
 ALL_CHECKS = (check_golden, check_brute_force, check_closed_forms, check_invariants, check_fw_vs_dijkstra,
-              check_negative_weights, check_dijkstra_csr)
+              check_negative_weights, check_dijkstra_csr, check_johnson_rows)
 
 
 def run_all(orc) -> list[str]:

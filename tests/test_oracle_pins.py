@@ -81,6 +81,11 @@ def test_networkx_third_opinion():
         assert np.array_equal(oracle.fw_i32(w).astype(np.int64), ref)
 
 
+def test_johnson_rows():
+    bad = pins.check_johnson_rows(oracle.default())
+    assert not bad, _fail_msg(bad)
+
+
 def test_dijkstra_csr():
     bad = pins.check_dijkstra_csr(oracle.default())
     assert not bad, _fail_msg(bad)
