@@ -306,3 +306,17 @@ def test_dense_rows_take_the_cta_partition():
     src = np.array([0, 1, 4500, 8999], dtype=np.int32)
     got = apsp.sssp_delta(rp, col, wt, torch.from_numpy(src).cuda())
     assert_i32_exact(got.cpu().numpy(), oracle.dijkstra_i32(w, src), "dense rows")
+
+
+def test_negative_weights_above_the_512_thread_limit():
+    # n = 17000 takes the 1024-thread search kernel; rows against the
+    # oracle's Johnson for sampled sources
+    n = 17000
+    w = graphgen.er_potential_i32(n, 0.002, 0, 1000, 2000, seed=77)
+    src = np.array([0, 1, 8500, 16999], dtype=np.int32)
+    ref = oracle.johnson_rows_i32(w, src)
+    assert ref is not None and (w[w < INF] < 0).any()
+    t = torch.from_numpy(w).cuda()
+    apsp.solve_sparse(t)
+    got = t[torch.from_numpy(src).long().cuda()].cpu().numpy()
+    assert_i32_exact(got, ref, "n=17000 negative weights")
