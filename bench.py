@@ -89,6 +89,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(dist, x: float, device) -> float:
+    """The largest x over all ranks (x itself without a process group): the
+    timed region of a multi-rank run is the slowest rank's."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, steps: int, work_per_step: float, seconds: float) -> float:
+    """Whole-job throughput: every rank does `steps` steps of `work_per_step`
+    units (replicas), in the slowest rank's `seconds`."""
+    return world * steps * work_per_step / seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -319,12 +337,9 @@ def ours(args, rank, world, local):
     phase_ms, phase_cnt = apsp.phase_timing_read()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, total_ms, dev)
     relax_per_step = float(n) ** 3
-    value = world * args.steps * relax_per_step / (total_ms * 1e-3)
+    value = whole_job_value(world, args.steps, relax_per_step, total_ms * 1e-3)
 
     # correctness spot check of the timed result: four oracle rows
     check = None
@@ -357,12 +372,9 @@ def ours(args, rank, world, local):
             apsp.solve_host(pinned)
             e2e_times.append(time.perf_counter() - t0)
         e2e_total = sum(e2e_times)
-        if dist is not None:
-            t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_total = float(t.item())
+        e2e_total = max_over_ranks(dist, e2e_total, dev)
         nbytes = n * n * w.itemsize
-        e2e = {"value": world * args.steps * relax_per_step / e2e_total, "unit": UNIT,
+        e2e = {"value": whole_job_value(world, args.steps, relax_per_step, e2e_total), "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "ms_per_step": e2e_total / args.steps * 1e3}
 
@@ -544,11 +556,8 @@ def ours_johnson(args, rank, world, local):
     search_ms, searches, kernels = apsp.sparse_timing_read()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps * float(n) ** 3 / (total_ms * 1e-3)
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    value = whole_job_value(world, args.steps, float(n) ** 3, total_ms * 1e-3)
 
     check = None
     if rank == 0:
@@ -575,12 +584,9 @@ def ours_johnson(args, rank, world, local):
             if it > 0:
                 e2e_times.append(time.perf_counter() - t0)
         e2e_total = sum(e2e_times)
-        if dist is not None:
-            t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_total = float(t.item())
+        e2e_total = max_over_ranks(dist, e2e_total, dev)
         nbytes = n * n * 4
-        e2e = {"value": world * args.steps * float(n) ** 3 / e2e_total, "unit": UNIT,
+        e2e = {"value": whole_job_value(world, args.steps, float(n) ** 3, e2e_total), "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
                "ms_per_step": e2e_total / args.steps * 1e3}
 
@@ -716,11 +722,8 @@ def ours_sssp(args, rank, world, local):
     search_ms, searches, kernels = apsp.sparse_timing_read()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps * m / (total_ms * 1e-3)
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    value = whole_job_value(world, args.steps, m, total_ms * 1e-3)
 
     check = None
     if rank == 0:
@@ -743,8 +746,8 @@ def ours_sssp(args, rank, world, local):
             torch.cuda.current_stream(dev).synchronize()
             if it > 0:
                 times.append(time.perf_counter() - t0)
-        e2e_total = sum(times)
-        e2e = {"value": world * args.steps * m / e2e_total, "unit": "TEPS", "h2d_bytes_per_step": 4,
+        e2e_total = max_over_ranks(dist, sum(times), dev)
+        e2e = {"value": whole_job_value(world, args.steps, m, e2e_total), "unit": "TEPS", "h2d_bytes_per_step": 4,
                "d2h_bytes_per_step": n * 4, "ms_per_step": e2e_total / args.steps * 1e3,
                "graph_h2d_bytes_once": int(row_ptr.nbytes + col.nbytes + w.nbytes)}
 
@@ -794,9 +797,14 @@ def ours_sssp(args, rank, world, local):
 # ------------------------------------------------------------------ out-of-core arm
 
 def ours_ooc(args, rank, world, local):
+    """One host matrix streamed through one GPU: under torchrun only rank 0
+    runs it (the other ranks exit without work)."""
     import torch
 
     import min_graph_gb300 as apsp
+
+    if rank != 0:
+        return
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
