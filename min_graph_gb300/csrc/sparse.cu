@@ -661,13 +661,20 @@ __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int 
             const int t = o + q * 32 + lane;
             x[q] = t < cnt ? __ldg(arcs + beg + t) : make_int2(0, -1);
         }
+        // the four targets' distances first, all in flight together: a value
+        // read before another relaxation lowers it is only larger (distances
+        // only decrease), so the check may try an atomic in vain, never skip a
+        // needed one
+        int32_t du[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) du[q] = x[q].y < 0 ? 0 : ld_cg_i32(dist + x[q].x);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (x[q].y < 0) continue;
             const uint32_t s = dv + (uint32_t)x[q].y;
             const int32_t nd = s >= (uint32_t)kUnreached ? kUnreached : (int32_t)s;
             const int u = x[q].x;
-            if (nd < ld_cg_i32(dist + u) && nd < atomicMin(dist + u, nd)) {
+            if (nd < du[q] && nd < atomicMin(dist + u, nd)) {
                 atomicOr(queued + (u >> 5), 1u << (u & 31));
                 atomicMin(wmin + (u >> 5), nd);
                 best = min(best, nd);
@@ -758,13 +765,16 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
                     d[q] = __shfl_sync(0xffffffffu, dv, pos);
                     x[q] = t < total ? __ldg(a.arcs + e) : make_int2(0, -1);
                 }
+                int32_t du[4];  // all four loads in flight before the atomics (see relax_run)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) du[q] = x[q].y < 0 ? 0 : ld_cg_i32(a.dist + x[q].x);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (x[q].y < 0) continue;
                     const uint32_t sum = d[q] + (uint32_t)x[q].y;
                     const int32_t nd = sum >= (uint32_t)kUnreached ? kUnreached : (int32_t)sum;
                     const int u = x[q].x;
-                    if (nd < ld_cg_i32(a.dist + u) && nd < atomicMin(a.dist + u, nd)) {
+                    if (nd < du[q] && nd < atomicMin(a.dist + u, nd)) {
                         atomicOr(a.queued + (u >> 5), 1u << (u & 31));
                         atomicMin(a.wmin + (u >> 5), nd);
                         best = min(best, nd);
