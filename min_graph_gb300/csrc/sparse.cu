@@ -550,13 +550,15 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
 // that other SMs write is read through L2 (ld.global.cg), never from a stale
 // L1 line.  Arc data is read-only and goes through the read-only path.  A
 // vertex with more than kGridBig arcs in the phase is not walked by its warp
-// alone: it goes to a per-CTA list that all warps of the CTA share out in
-// 128-arc pieces after their own batches.
+// alone: its arcs go, in segments of kGridBig, to a grid-wide list.  The
+// phase's barrier then says (OR) whether the list is empty; if not, every
+// warp of the grid takes segments from it through an atomic cursor, and a
+// second barrier closes the phase.  A hub of an R-MAT graph (up to 10^5 -
+// 10^6 arcs) is so spread over the whole GPU.
 
 constexpr int kGridThreads = 512;
 constexpr int kGridWarps = kGridThreads / 32;
 constexpr int kGridBig = 1024;
-constexpr int kGridBigCap = 128;
 
 struct GridCtrl {
     int any[3];          // OR slots, by barrier index mod 3
@@ -564,7 +566,9 @@ struct GridCtrl {
     unsigned arrive;     // barrier arrivals
     unsigned gen;        // barrier generation
     int err;             // 1: a barrier wait ran out
-    int pad[7];
+    int big_count;       // segments on the grid-wide list in this phase
+    int big_cursor;      // segments taken from it
+    int pad[5];
 };
 
 struct GridArgs {
@@ -579,6 +583,8 @@ struct GridArgs {
     uint32_t* front;
     uint32_t* rset;
     GridCtrl* ctrl;
+    int4* big;       // grid-wide list of hub segments: (dv, begin, count, -)
+    int big_cap;
     unsigned long long timeout_ns;
     int inject;  // test hook: CTA 0 leaves before the first barrier
 };
@@ -644,11 +650,6 @@ __device__ bool grid_reduce(const GridArgs& a, int& k, int any_in, int32_t min_i
     return ok;
 }
 
-struct GridBig {
-    int4 e[kGridBigCap];  // (dv, begin, count, -)
-    int count;
-};
-
 // Relax `cnt` arcs from `beg` for a vertex at distance dv, 32 lanes of a warp
 // striding over them, up to 4 loads in flight.
 __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int beg, int cnt, uint32_t dv,
@@ -686,11 +687,11 @@ __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int 
 
 // Relax the light (kLight) or heavy arcs of every vertex in the bitmap `set`
 // (global), clearing it.  Batches of 32 vertices as in the CTA search; a
-// vertex with more than kGridBig arcs goes to the CTA's list `big` (its warp
-// walks it itself when the list is full), and the CTA's warps share out the
-// list once all batches are done.
+// vertex with more than kGridBig arcs goes to the grid-wide list in segments
+// of kGridBig (its warp walks it itself if the list is full), and `pushed`
+// says whether this lane put any there.
 template <bool kLight>
-__device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
+__device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
     int32_t best = INT_MAX;
@@ -731,10 +732,13 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
                 }
                 dv = (uint32_t)ld_cg_i32(a.dist + v);
                 if (cnt > kGridBig) {
-                    const int slot = atomicAdd(&big.count, 1);
-                    if (slot < kGridBigCap) {
-                        big.e[slot] = make_int4((int)dv, beg, cnt, 0);
+                    const int nseg = (cnt + kGridBig - 1) / kGridBig;
+                    const int slot = atomicAdd(&a.ctrl->big_count, nseg);
+                    if (slot + nseg <= a.big_cap) {
+                        for (int q = 0; q < nseg; ++q)
+                            a.big[slot + q] = make_int4((int)dv, beg + q * kGridBig, min(kGridBig, cnt - q * kGridBig), 0);
                         cnt = 0;
+                        pushed = 1;
                     }
                 }
             }
@@ -783,28 +787,51 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, GridBig& big) {
             }
         }
     }
-    // the CTA's big vertices, in 128-arc pieces shared out over its warps
-    __syncthreads();
-    const int nbig = min(big.count, kGridBigCap);
-    int piece = 0;
-    for (int b = 0; b < nbig; ++b) {
-        const int4 e = big.e[b];
-        for (int o = 0; o < e.z; o += 128, ++piece) {
-            if (piece % kGridWarps != warp) continue;
-            best = min(best, relax_run(a.arcs, e.y + o, min(128, e.z - o), (uint32_t)e.x, a.dist, a.queued,
-                                       a.wmin, lane));
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) big.count = 0;
     return best;
+}
+
+// After the barrier that ends a phase's batches: every warp takes hub
+// segments from the grid-wide list until it is empty (the count is final by
+// then).
+__device__ int32_t drain_grid_list(const GridArgs& a) {
+    const int lane = threadIdx.x & 31;
+    const int count = min(*reinterpret_cast<volatile int*>(&a.ctrl->big_count), a.big_cap);
+    int32_t best = INT_MAX;
+    for (;;) {
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(&a.ctrl->big_cursor, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx >= count) break;
+        const int4 e = a.big[idx];
+        best = min(best, relax_run(a.arcs, e.y, e.z, (uint32_t)e.x, a.dist, a.queued, a.wmin, lane));
+    }
+    return best;
+}
+
+// The rest of a phase once its batches are done: the closing barrier, or,
+// when some warp put hub segments on the grid-wide list, a barrier, the
+// list shared out over the grid, and a second barrier.  CTA 0 empties the
+// list after that: the next push comes only after the next selection's
+// barrier.  `best` in: this lane's least successful relaxation; out: the
+// MIN over the grid.  Returns false when the search must stop.
+__device__ bool close_phase(const GridArgs& a, int& k, int pushed, int32_t in_min, int32_t& out_min) {
+    int any_big;
+    if (!grid_reduce(a, k, pushed, in_min, any_big, out_min)) return false;
+    if (!any_big) return true;
+    const int32_t b = drain_grid_list(a);
+    int unused;
+    int32_t m2;
+    if (!grid_reduce(a, k, 0, b, unused, m2)) return false;
+    out_min = min(out_min, m2);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.ctrl->big_count = 0;
+        a.ctrl->big_cursor = 0;
+    }
+    return true;
 }
 
 __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) {
     if (a.inject && blockIdx.x == 0) return;  // test hook (apsp_debug_inject_grid_timeout)
-    __shared__ GridBig big;
-    if (threadIdx.x == 0) big.count = 0;
-    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
     int k = 0;  // barrier index, the same in every CTA
@@ -868,13 +895,14 @@ __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) 
             int32_t unused;
             if (!grid_reduce(a, k, any, INT_MAX, any_g, unused)) return;
             if (!any_g) break;
-            expand_grid<true>(a, a.front, big);
-            if (!grid_reduce(a, k, 0, INT_MAX, any_g, unused)) return;
+            int pushed = 0;
+            expand_grid<true>(a, a.front, pushed);
+            if (!close_phase(a, k, pushed, INT_MAX, unused)) return;
         }
-        const int32_t hbest = expand_grid<false>(a, a.rset, big);
-        int any_g;
+        int pushed = 0;
+        const int32_t hbest = expand_grid<false>(a, a.rset, pushed);
         int32_t next;
-        if (!grid_reduce(a, k, 0, min(beyond, hbest), any_g, next)) return;
+        if (!close_phase(a, k, pushed, min(beyond, hbest), next)) return;
         if (next == INT_MAX) break;
         dmin = next;
     }
@@ -901,6 +929,8 @@ __global__ void grid_init_kernel(GridArgs a, int src) {
         c->arrive = 0u;
         c->gen = 0u;
         c->err = 0;
+        c->big_count = 0;
+        c->big_cursor = 0;
     }
 }
 
@@ -1253,13 +1283,19 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
 }
 
 // Grid-search buffer: [ctrl 256 B | flags 256 B | (row_ptr copy) | nlight |
-// queued | wmin | front | rset | arcs | big-vertex list], each section
-// 256-byte aligned.  flags: [0..2] weight range, [4] row_ptr check, [6]
-// big-vertex count.
+// queued | wmin | front | rset | arcs | partition's big-vertex list | hub
+// segment list], each section 256-byte aligned.  flags: [0..2] weight range,
+// [4] row_ptr check, [6] big-vertex count.  The segment list holds at most
+// one phase's hub segments: fewer than m / kGridBig full ones plus one
+// partial one per hub, itself more than kGridBig arcs, so 2 m / kGridBig + 16
+// entries suffice.
+int grid_seg_cap(long long m) { return (int)(2 * (m / kGridBig) + 16); }
+
 size_t grid_bytes(int n, long long m, bool own_rp) {
     const size_t nw = (size_t)(n + 31) / 32;
     return 512 + (own_rp ? align256((size_t)(n + 1) * 8) : 0) + 2 * align256((size_t)n * 4) +
-           4 * align256(nw * 4) + align256((size_t)(m > 0 ? m : 1) * 8);
+           4 * align256(nw * 4) + align256((size_t)(m > 0 ? m : 1) * 8) +
+           align256((size_t)grid_seg_cap(m) * sizeof(int4));
 }
 
 // Check the graph, choose delta, lay out `buf` and partition the arcs into
@@ -1289,6 +1325,9 @@ apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t*
     int2* arcs = reinterpret_cast<int2*>(buf + off);
     off += align256((size_t)(m > 0 ? m : 1) * 8);
     int32_t* biglist = reinterpret_cast<int32_t*>(buf + off);
+    off += align256((size_t)n * 4);
+    a.big = reinterpret_cast<int4*>(buf + off);
+    a.big_cap = grid_seg_cap(m);
     a.nlight = nlight;
     a.arcs = arcs;
     a.n = n;
