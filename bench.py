@@ -74,6 +74,7 @@ def parse():
     ap.add_argument("--workload", default="ba16384", choices=sorted(graphgen.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--threads", type=int, default=0, help="host threads for the oracle (0: all cores)")
     ap.add_argument("--algo", choices=["fw", "johnson", "sssp", "ooc"], default="fw")
     ap.add_argument("--block", type=int, default=4096, help="super-block K for --algo ooc (0: from the budget)")
     ap.add_argument("--device-bytes", type=int, default=0, help="device budget for --algo ooc (0: 70%% of free)")
@@ -203,9 +204,12 @@ def reference_arm(args, rank):
 
     w = graphgen.make(args.workload)
     n = w.shape[0]
-    d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
+    is_i32 = w.dtype == np.int32
+    d = (np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True) if is_i32
+         else np.array(w, dtype=np.float64, copy=True))
     orc = oracle.default()
-    thr = oracle.default_threads()
+    thr = args.threads or oracle.default_threads()
+    fw_steps = orc.fw_i32_steps if is_i32 else orc.fw_f64_steps
     # Each step runs chunks of k-steps (continuing, wrapping around n) until
     # about 2.5 s have passed, so that W + K steps finish in a few minutes.
     chunk, k = 8, 0
@@ -216,7 +220,7 @@ def reference_arm(args, rank):
         while dt < 2.5:
             kk = min(n, k + chunk)
             t0 = time.perf_counter()
-            orc.fw_i32_steps(d, k, kk, threads=thr)
+            fw_steps(d, k, kk, threads=thr)
             dt += time.perf_counter() - t0
             done += kk - k
             k = kk % n
@@ -226,12 +230,13 @@ def reference_arm(args, rank):
     tot = sum(times)
     value = sum(relax) / tot
     ks = int(round(sum(relax) / len(relax) / (float(n) * n)))
-    sample = (f"about {ks} Floyd-Warshall k-steps of the untiled triple loop on the full "
-              f"n={n} {args.workload} matrix per step (~2.5 s, {thr} threads)")
+    sample = (f"about {ks} Floyd-Warshall k-steps of the untiled triple loop "
+              f"({'int32' if is_i32 else 'fp64'}) on the full n={n} {args.workload} matrix per step "
+              f"(~2.5 s, {thr} threads), n^3 rate extrapolated from them")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32" if is_i32 else "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload),
                    "sample": sample},
@@ -417,6 +422,22 @@ def ours(args, rank, world, local):
                 "frac_at_load_clock": (achieved / (peak_tops * f_load / f_max)) if f_load else None,
                 "avg_launch_ms": p3_ms, "launches": p3_launches,
                 "phase_share": [m / sum(phase_ms) for m in phase_ms] if sum(phase_ms) > 0 else None}
+        if not fused and phase_cnt[0] > 0 and phase_cnt[1] > 0:
+            # the three-kernel schedule times phases 1 and 2 apart: their HBM
+            # rates, algorithmic bytes per launch (phase 1: the primary tile
+            # read and written; phase 2: each of the 2(nb-1) panel tiles read,
+            # written back and written to the workspace panel)
+            hbm = peaks().get("hbm_gbs") or 6800.0
+            tile = TB * TB * w.itemsize
+            p1_ms = phase_ms[0] / phase_cnt[0]
+            p2_ms = phase_ms[1] / phase_cnt[1]
+            p1_gbs = 2 * tile / (p1_ms * 1e-3) / 1e9
+            p2_gbs = 2 * (nb - 1) * 3 * tile / (p2_ms * 1e-3) / 1e9
+            roof["phases_1_2"] = {
+                "phase1": {"ms_per_launch": p1_ms, "GB/s": p1_gbs, "frac_hbm": p1_gbs / hbm},
+                "phase2": {"ms_per_launch": p2_ms, "GB/s": p2_gbs, "frac_hbm": p2_gbs / hbm},
+                "hbm_peak_gbs": hbm}
+        roof["solve_hbm_GBps"] = 2.0 * w.itemsize * float(n) * n * nb / (total_ms / args.steps * 1e-3) / 1e9
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and dtype == torch.int32:

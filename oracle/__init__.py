@@ -79,6 +79,8 @@ def bind(path: str):
     lib.oracle_fw_i32_steps.restype = i32
     lib.oracle_fw_f64.argtypes = [vp, i64, i64, i32]
     lib.oracle_fw_f64.restype = i32
+    lib.oracle_fw_f64_steps.argtypes = [vp, i64, i64, i64, i64, i32]
+    lib.oracle_fw_f64_steps.restype = i32
     lib.oracle_dijkstra_i32.argtypes = [vp, i64, i64, vp, i64, i32, vp, i32]
     lib.oracle_dijkstra_i32.restype = i32
     lib.oracle_dijkstra_f32.argtypes = [vp, i64, i64, vp, i64, i32, vp, i32]
@@ -156,6 +158,12 @@ class Oracle:
         d = np.array(w[:n, :n], dtype=np.float64, order="C", copy=True)
         _check(self.lib.oracle_fw_f64(d.ctypes.data, n, n, threads), "fw_f64")
         return d
+
+    def fw_f64_steps(self, d: np.ndarray, k_begin: int, k_end: int, threads: int = 1) -> None:
+        """Floyd-Warshall steps k_begin..k_end-1 in place on a float64 matrix."""
+        d = _as_matrix(d, np.float64)
+        _check(self.lib.oracle_fw_f64_steps(d.ctypes.data, d.shape[0], d.shape[1], k_begin, k_end, threads),
+               "fw_f64_steps")
 
     def dijkstra_i32(self, w: np.ndarray, sources, reverse: bool = False,
                      threads: int | None = None, n: int | None = None) -> np.ndarray:

@@ -126,6 +126,27 @@ int oracle_fw_f64(double* d, int64_t n, int64_t ld, int threads) {
     return 0;
 }
 
+/* Steps k in [k_begin, k_end) of oracle_fw_f64 only (to time a bounded
+ * sample of an fp32 workload). */
+int oracle_fw_f64_steps(double* d, int64_t n, int64_t ld, int64_t k_begin, int64_t k_end, int threads) {
+    if (n < 0 || ld < n || k_begin < 0 || k_end > n || (n > 0 && !d)) return -1;
+    (void)threads;
+    for (int64_t k = k_begin; k < k_end; ++k) {
+        const double* rowk = d + k * ld;
+#pragma omp parallel for schedule(static) num_threads(threads > 0 ? threads : 1) if (threads > 1)
+        for (int64_t i = 0; i < n; ++i) {
+            double* rowi = d + i * ld;
+            double dik = rowi[k];
+            if (isinf(dik)) continue;
+            for (int64_t j = 0; j < n; ++j) {
+                double s = dik + rowk[j];
+                if (s < rowi[j]) rowi[j] = s;
+            }
+        }
+    }
+    return 0;
+}
+
 /* ---------------- graph in adjacency form ---------------- */
 
 typedef struct {

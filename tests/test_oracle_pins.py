@@ -68,6 +68,16 @@ def test_fw_steps_compose():
     assert np.array_equal(d, orc.fw_i32(w))
 
 
+def test_fw_f64_steps_compose():
+    """The fp64 steps [0,a) then [a,n) equal the full fp64 run."""
+    w = graphgen.er_f32(150, 0.05, 3)
+    orc = oracle.default()
+    d = w.astype(np.float64)
+    orc.fw_f64_steps(d, 0, 60)
+    orc.fw_f64_steps(d, 60, 150, threads=2)
+    assert np.array_equal(d, orc.fw_f64(w))
+
+
 def test_networkx_third_opinion():
     nx = pytest.importorskip("networkx")
     for seed, n, p in ((1, 60, 0.05), (2, 90, 0.1)):
