@@ -201,10 +201,15 @@ size_t ooc_elems(int n, int K) {
     return 5 * (size_t)K * K + 2 * (size_t)K * npad;
 }
 
+// The copy-in and copy-out streams of the block ring and their events.  On
+// every exit, error paths included, the streams are drained first, so the
+// device buffer is never freed under a copy still in flight.
 struct Streams {
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t loaded[3] = {}, done[3] = {}, freed[3] = {};
     ~Streams() {
+        if (in) cudaStreamSynchronize(in);
+        if (out) cudaStreamSynchronize(out);
         for (int q = 0; q < 3; ++q) {
             if (loaded[q]) cudaEventDestroy(loaded[q]);
             if (done[q]) cudaEventDestroy(done[q]);

@@ -1142,10 +1142,9 @@ apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int3
 // Partition the arcs against delta, then one persistent search CTA per
 // resident slot.  512 threads a CTA while at least two CTAs fit an SM (n up
 // to about 24K), else 1024 threads in one CTA.
-apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m,
-                          const int32_t* sources, int nsrc, int32_t delta, const long long* h, int32_t* out,
-                          long long ldo, const Work& wk, cudaStream_t s) {
-    (void)m;
+apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, const int32_t* sources,
+                          int nsrc, int32_t delta, const long long* h, int32_t* out, long long ldo, const Work& wk,
+                          cudaStream_t s) {
     apsp_status_t prc = partition_arcs(rp, col, w, n, delta, wk.arcs, wk.nlight, wk.biglist, wk.bigcount, s);
     if (prc != APSP_OK) return prc;
     cudaError_t e;
@@ -1253,7 +1252,7 @@ apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, i
         if (rc != APSP_OK) return rc;
     }
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(rp, col, wuse, n, m, nullptr, n, delta, huse, out, ld, wk, s);
+    return launch_sssp(rp, col, wuse, n, nullptr, n, delta, huse, out, ld, wk, s);
 }
 
 // CSR of a dense matrix into st.rp / st.body; returns m.
@@ -1592,7 +1591,7 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
     if (rc != APSP_OK) return rc;
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(row_ptr, col_idx, w, n, m, sources, nsrc, delta, nullptr, out, ldo, wk, s);
+    return launch_sssp(row_ptr, col_idx, w, n, sources, nsrc, delta, nullptr, out, ldo, wk, s);
 }
 
 apsp_status_t apsp_johnson_csr_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,
