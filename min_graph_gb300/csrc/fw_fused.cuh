@@ -26,9 +26,13 @@
 // only.
 //
 // Each CTA is one producer warp (an elected thread takes items, waits for
-// their inputs, and issues TMA loads) and eight consumer warps (the
-// arithmetic, on the tile-product core of mm_core.cuh).
-//   phase-3 tile:  C <- D tile; A slabs <- column panel; B slabs <- row panel
+// their inputs, and issues TMA loads and reductions) and eight consumer
+// warps (the arithmetic, on the tile-product core of mm_core.cuh).
+//   phase-3 tile:  A slabs <- column panel; B slabs <- row panel.  int32: the
+//                  accumulators start at INF, the consumers stage the result
+//                  in the C buffer, and the producer merges it into D with a
+//                  TMA min-reduction in L2 (D is never loaded into the SM).
+//                  fp32: C <- D tile first, plain stores at the end.
 //   row panel:     C <- D tile (also the B operand, read in shared memory);
 //                  A slabs <- transposed closed primary tile
 //   column panel:  C <- D tile; the consumers write its transpose into the
@@ -54,6 +58,12 @@ constexpr uint32_t FZ_C = TB * TB * 4;          // 64 KiB
 constexpr uint32_t FZ_MISC = 4096;              // barriers, item slots, phase-1 buffers
 constexpr size_t kFusedSmem = 1024 + FZ_C + (size_t)FZ_STAGES * FZ_STAGE + FZ_MISC;
 constexpr int FZ_NAMED_BAR = 1;                 // consumer-only named barrier id
+
+// Phase-3 epilogue by TMA reduction (int32): D <- min(D, tile) is a signed
+// 32-bit minimum in L2.  The bulk tensor reduction has no fp32 minimum, so
+// fp32 tiles load D first and store the result with plain stores.
+template <typename T>
+constexpr bool kMergeEpilogueFor = std::is_same<T, int32_t>::value;
 
 enum : int { kItemP3 = 0, kItemP1 = 1, kItemP2Row = 2, kItemP2Col = 3 };
 enum : int { kCritNone = 0, kCritDiag = 1, kCritRow = 2, kCritCol = 3 };
@@ -199,10 +209,13 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     const uint32_t bar_empty = bar_full + 8 * FZ_STAGES;
     const uint32_t bar_cfull = bar_empty + 8 * FZ_STAGES;
     const uint32_t bar_cempty = bar_cfull + 8;
+    const uint32_t bar_staged = bar_cempty + 8;  // merge epilogue: tile staged in the C buffer
+    const uint32_t bar_sfree = bar_staged + 8;   // merge epilogue: staged tile read by the reduction
     const int tid = threadIdx.x;
     const int rn = r + 1;
     const int x = fused_head(nb, gridDim.x);
     int* err = ptrs.err;
+    constexpr bool kMergeEpilogue = kMergeEpilogueFor<T>;
 
     if (tid == 0) {
         for (int s = 0; s < FZ_STAGES; ++s) {
@@ -211,6 +224,8 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         }
         mbar_init(bar_cfull, 1);
         mbar_init(bar_cempty, FZ_CONSUMERS / 32);
+        mbar_init(bar_staged, FZ_CONSUMERS / 32);
+        mbar_init(bar_sfree, 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -224,6 +239,39 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         uint32_t g = 0;
         int it = 0;
         bool ok = true;
+        // Merge epilogue: the phase-3 item whose tile the consumers stage in
+        // the C buffer, still to be merged into D, and the merges issued.
+        bool pend = false;
+        FusedItem pw;
+        pw.kind = kItemP3;
+        pw.I = pw.J = 0;
+        pw.crit = kCritNone;
+        uint32_t merges = 0;
+        // Merge the pending tile: D <- min(D, staged tile) by a TMA reduction
+        // in L2.  A critical tile's flag is set once the reduction's writes
+        // are complete; otherwise it is enough that the buffer has been read.
+        auto merge_pending = [&]() -> bool {
+            if constexpr (!kMergeEpilogue) return true;
+            if (!pend) return true;
+            pend = false;
+            if (!mbar_wait_bounded(bar_staged, merges & 1, err, timeout_ns)) return false;
+            tma_reduce_min_2d(&maps.c, pw.J * TB, pw.I * TB, cdst);
+            bulk_commit();
+            if (pw.crit != kCritNone) {
+                bulk_wait_all();
+                int* f = pw.crit == kCritDiag ? ptrs.flag_diag
+                         : pw.crit == kCritRow ? ptrs.flag_row + pw.J
+                                               : ptrs.flag_col + pw.I;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                atomicExch(f, rn);
+            } else {
+                bulk_wait_read_all();
+            }
+            mbar_arrive(bar_sfree);
+            ++merges;
+            return true;
+        };
         for (;;) {
             const int l = atomicAdd(ptrs.counters + rn, 1);
             const bool stop = l >= nitems;
@@ -231,8 +279,12 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             w.kind = kItemP3;
             w.I = w.J = 0;
             w.crit = kCritNone;
-            if (!stop) {
-                w = fused_item(l, r, nb, x);
+            if (!stop) w = fused_item(l, r, nb, x);
+            const bool merged = kMergeEpilogue && !stop && w.kind == kItemP3;
+            // Phase 1 and 2 items need the C buffer and may wait for the
+            // pending tile's flag: merge it first.  So does the end.
+            if (!merged) ok = merge_pending();
+            if (ok && !stop) {
                 if (w.kind == kItemP1 && r >= 0)
                     ok = flag_wait(ptrs.flag_diag, rn, err, timeout_ns);
                 else if (w.kind == kItemP2Row)
@@ -249,8 +301,12 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 break;
             }
             slots[it & 1] = l;
-            mbar_arrive_expect_tx(bar_cfull, FZ_C);
-            tma_load_2d(cdst, &maps.c, w.J * TB, w.I * TB, bar_cfull);
+            if (merged) {
+                mbar_arrive(bar_cfull);  // no C tile: the consumers start from INF
+            } else {
+                mbar_arrive_expect_tx(bar_cfull, FZ_C);
+                tma_load_2d(cdst, &maps.c, w.J * TB, w.I * TB, bar_cfull);
+            }
             ++it;
             if (w.kind == kItemP1) continue;  // no slabs
             for (int s = 0; s < TB / KS; ++s) {
@@ -259,8 +315,9 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                     ok = false;
                     break;
                 }
-                if (inject && g == 0 && blockIdx.x == 0) {
-                    // Test hook: this slab is never issued, so the consumers'
+                if (inject && l == 0 && s == 0) {
+                    // Test hook: the first slab of item 0 (a phase-3 tile in
+                    // every launch r >= 0) is never issued, so the consumers'
                     // bounded wait on it must run out (APSP_ETIMEOUT).
                     ++g;
                     continue;
@@ -280,6 +337,14 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 ++g;
             }
             if (!ok) break;
+            if (merged) {
+                // this item's slabs are issued: merge the previous phase-3
+                // tile (its consumers are finishing it now)
+                ok = merge_pending();
+                pw = w;
+                pend = true;
+                if (!ok) break;
+            }
         }
         (void)nbuf;
         if (!ok) {
@@ -289,6 +354,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                                   false);
             if (it > 0) mbar_wait_bounded(bar_cfull, (it - 1) & 1, err, timeout_ns, false);
         }
+        bulk_wait_all();  // no reduction may still read shared memory or write D
         return;
     }
 
@@ -297,12 +363,49 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     const int lane = tid & 31;
     const int pb = r & 1, nbuf = rn & 1;
     uint32_t g = 0;
+    uint32_t staged = 0;  // merge epilogue: tiles staged so far
     for (int it = 0;; ++it) {
         if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
         const int l = slots[it & 1];
         if (l < 0) return;
         const FusedItem w = fused_item(l, r, nb, x);
         const int row0 = w.I * TB, col0 = w.J * TB;
+
+        if (kMergeEpilogue && w.kind == kItemP3) {
+            // ------------------------- phase 3 (round r), merge epilogue
+            // The accumulators start at INF instead of the D tile; the tile
+            // is staged in the C buffer and the producer's TMA reduction
+            // takes D <- min(D, tile) in L2.  min(D, INF, products) equals
+            // min(clamp(D), products), so this also clamps inputs above INF.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);  // the slot has been read
+            T acc[8][8];
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri)
+#pragma unroll
+                for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::inf();
+            for (int s = 0; s < TB / KS; ++s, ++g) {
+                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
+                if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
+                const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
+                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+            }
+            // the previous staged tile must have been read by its reduction
+            if (staged > 0 && !mbar_wait_bounded(bar_sfree, (staged - 1) & 1, err, timeout_ns)) return;
+#pragma unroll
+            for (int ri = 0; ri < 8; ++ri) {
+                vstore4(cbuf + L.row(ri) * TB + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                vstore4(cbuf + L.row(ri) * TB + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+            }
+            // the reduction reads the buffer through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_staged);
+            ++staged;
+            continue;
+        }
 
         if (w.kind == kItemP1) {
             // ------------------------------------------------ phase 1 (round rn)

@@ -94,4 +94,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         : "memory");
 }
 
+// 2-D tiled bulk tensor reduction shared -> global: every in-bounds element
+// of the box becomes min(global, shared), performed in L2, with the element
+// type of the tensor map (INT32 maps: signed 32-bit minimum).  Elements of
+// the box outside the tensor are not written.  Tracked by the issuing
+// thread's bulk async-groups.
+__device__ __forceinline__ void tma_reduce_min_2d(const CUtensorMap* tm, int x, int y, uint32_t src) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.min.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+        "r"(x), "r"(y), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Every committed bulk group has completed (its global writes are done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 }  // namespace apsp
