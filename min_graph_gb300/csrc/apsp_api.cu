@@ -324,6 +324,13 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
         const unsigned long long pitch = (unsigned long long)npad * sizeof(T);
         bool ok = true;
         f.maps.c = a.tm_c;
+        // Phase-3 tiles merge into D by a signed 32-bit min-reduction.  For
+        // fp32 that is the order of the values too: within the contract
+        // every entry is +0, positive or +inf (a -0.0 input acts as zero).
+        if (is_float)
+            ok = encode_2d(&f.maps.cmin, false, d, n, n, (unsigned long long)ld * sizeof(T), kTB, kTB);
+        else
+            f.maps.cmin = a.tm_c;
         for (int b = 0; b < 2; ++b) {
             ok = ok && encode_2d(&f.maps.rowp[b], is_float, f.ptrs.rowp[b], npad, kTB, pitch, kTB, ks);
             ok = ok && encode_2d(&f.maps.colpT[b], is_float, f.ptrs.colpT[b], npad, kTB, pitch, kTB, ks);

@@ -28,11 +28,10 @@
 // Each CTA is one producer warp (an elected thread takes items, waits for
 // their inputs, and issues TMA loads and reductions) and eight consumer
 // warps (the arithmetic, on the tile-product core of mm_core.cuh).
-//   phase-3 tile:  A slabs <- column panel; B slabs <- row panel.  int32: the
+//   phase-3 tile:  A slabs <- column panel; B slabs <- row panel.  The
 //                  accumulators start at INF, the consumers stage the result
 //                  in the C buffer, and the producer merges it into D with a
 //                  TMA min-reduction in L2 (D is never loaded into the SM).
-//                  fp32: C <- D tile first, plain stores at the end.
 //   row panel:     C <- D tile (also the B operand, read in shared memory);
 //                  A slabs <- transposed closed primary tile
 //   column panel:  C <- D tile; the consumers write its transpose into the
@@ -59,11 +58,12 @@ constexpr uint32_t FZ_MISC = 4096;              // barriers, item slots, phase-1
 constexpr size_t kFusedSmem = 1024 + FZ_C + (size_t)FZ_STAGES * FZ_STAGE + FZ_MISC;
 constexpr int FZ_NAMED_BAR = 1;                 // consumer-only named barrier id
 
-// Phase-3 epilogue by TMA reduction (int32): D <- min(D, tile) is a signed
-// 32-bit minimum in L2.  The bulk tensor reduction has no fp32 minimum, so
-// fp32 tiles load D first and store the result with plain stores.
-template <typename T>
-constexpr bool kMergeEpilogueFor = std::is_same<T, int32_t>::value;
+// Phase-3 epilogue by TMA reduction: D <- min(D, tile) is a signed 32-bit
+// minimum in L2, through an INT32-typed tensor map of D (the bulk tensor
+// reduction has no fp32 minimum).  For fp32 the integer order of the bit
+// patterns is the order of the values, because within the library's
+// contract every entry is +0, a positive float or +inf (a -0.0 input is the
+// smallest pattern and acts as zero).
 
 enum : int { kItemP3 = 0, kItemP1 = 1, kItemP2Row = 2, kItemP2Col = 3 };
 enum : int { kCritNone = 0, kCritDiag = 1, kCritRow = 2, kCritCol = 3 };
@@ -215,7 +215,6 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     const int rn = r + 1;
     const int x = fused_head(nb, gridDim.x);
     int* err = ptrs.err;
-    constexpr bool kMergeEpilogue = kMergeEpilogueFor<T>;
 
     if (tid == 0) {
         for (int s = 0; s < FZ_STAGES; ++s) {
@@ -251,11 +250,10 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         // in L2.  A critical tile's flag is set once the reduction's writes
         // are complete; otherwise it is enough that the buffer has been read.
         auto merge_pending = [&]() -> bool {
-            if constexpr (!kMergeEpilogue) return true;
             if (!pend) return true;
             pend = false;
             if (!mbar_wait_bounded(bar_staged, merges & 1, err, timeout_ns)) return false;
-            tma_reduce_min_2d(&maps.c, pw.J * TB, pw.I * TB, cdst);
+            tma_reduce_min_2d(&maps.cmin, pw.J * TB, pw.I * TB, cdst);
             bulk_commit();
             if (pw.crit != kCritNone) {
                 bulk_wait_all();
@@ -280,7 +278,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             w.I = w.J = 0;
             w.crit = kCritNone;
             if (!stop) w = fused_item(l, r, nb, x);
-            const bool merged = kMergeEpilogue && !stop && w.kind == kItemP3;
+            const bool merged = !stop && w.kind == kItemP3;
             // Phase 1 and 2 items need the C buffer and may wait for the
             // pending tile's flag: merge it first.  So does the end.
             if (!merged) ok = merge_pending();
@@ -371,8 +369,8 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         const FusedItem w = fused_item(l, r, nb, x);
         const int row0 = w.I * TB, col0 = w.J * TB;
 
-        if (kMergeEpilogue && w.kind == kItemP3) {
-            // ------------------------- phase 3 (round r), merge epilogue
+        if (w.kind == kItemP3) {
+            // ------------------------------------------------ phase 3 (round r)
             // The accumulators start at INF instead of the D tile; the tile
             // is staged in the C buffer and the producer's TMA reduction
             // takes D <- min(D, tile) in L2.  min(D, INF, products) equals
@@ -492,28 +490,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::clamp(acc[ri][ci]);
         }
 
-        if (w.kind == kItemP3) {
-            // ------------------------------------------------ phase 3 (round r)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_cempty);
-            for (int s = 0; s < TB / KS; ++s, ++g) {
-                const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
-                if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
-                const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
-                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * st);
-            }
-#pragma unroll
-            for (int ri = 0; ri < 8; ++ri) {
-                const int i = row0 + L.row(ri);
-                gstore4(D, ld, n, i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                gstore4(D, ld, n, i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
-            }
-            if (w.crit == kCritDiag) flag_signal(ptrs.flag_diag, rn);
-            else if (w.crit == kCritRow) flag_signal(ptrs.flag_row + w.J, rn);
-            else if (w.crit == kCritCol) flag_signal(ptrs.flag_col + w.I, rn);
-        } else if (w.kind == kItemP2Row) {
+        if (w.kind == kItemP2Row) {
             // -------------------------------- phase 2, row panel tile (rn, J)
             // B is the tile itself: put the clamped, edge-masked values back in
             // the shared buffer, then run the product over A slabs (P^T).

@@ -36,6 +36,7 @@ struct RoundArgs {
 // Tensor maps and buffers of the round-fused schedule (fw_fused.cuh).
 struct FusedMaps {
     CUtensorMap c;          // D: n x n, box TB x TB
+    CUtensorMap cmin;       // the same view of D typed INT32: the phase-3 min-reduction's element type
     CUtensorMap rowp[2];    // row panel buffers (alternate rounds): TB x npad, box KS x TB
     CUtensorMap colpT[2];   // transposed column panel buffers
     CUtensorMap prim;       // closed primary tile TB x TB, box KS x TB
