@@ -166,6 +166,15 @@ bool persistent_phase3_allowed() {
     return !(v && std::strcmp(v, "cpasync") == 0);
 }
 
+// Items per phase-3 tile along k in the fused schedule: the size-based
+// choice (fused_split), unless APSP_FUSED_SPLIT=1|2|4 forces one.
+int fused_split_for(int nb, int sms) {
+    const char* v = std::getenv("APSP_FUSED_SPLIT");
+    if (v && (std::strcmp(v, "1") == 0 || std::strcmp(v, "2") == 0 || std::strcmp(v, "4") == 0))
+        return v[0] - '0';
+    return apsp::fused_split(nb, sms);
+}
+
 // APSP_P3_COLS=4|8 picks the persistent phase 3's accumulator columns per
 // thread (512 or 256 consumer threads); the default is kDefaultP3Cols.
 constexpr int kDefaultP3Cols = 8;
@@ -319,6 +328,8 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
         f.ptrs.flag_row = flags + 2;
         f.ptrs.flag_col = flags + 2 + nb;
         f.ptrs.counters = flags + 2 + 2 * nb;
+        f.ptrs.parts = flags + 3 + 3 * nb;
+        f.split = fused_split_for(nb, st.sms);
         f.ptrs.err = a.err;
         const int ks = apsp::phase3_slab_rows();
         const unsigned long long pitch = (unsigned long long)npad * sizeof(T);
@@ -338,9 +349,11 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
         ok = ok && encode_2d(&f.maps.prim, is_float, a.prim, kTB, kTB, kTB * sizeof(T), kTB, ks);
         ok = ok && encode_2d(&f.maps.primT, is_float, a.primT, kTB, kTB, kTB * sizeof(T), kTB, ks);
         if (ok) {
-            // flags start at -1 (no round stamped yet), counters at 0
+            // flags start at -1 (no round stamped yet), item counters and
+            // critical-part counts at 0
             e = cudaMemsetAsync(flags, 0xFF, (size_t)(2 + 2 * nb) * sizeof(int), s);
-            if (e == cudaSuccess) e = cudaMemsetAsync(f.ptrs.counters, 0, (size_t)(nb + 1) * sizeof(int), s);
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(f.ptrs.counters, 0, (size_t)(nb + 1 + 2 * nb + 1) * sizeof(int), s);
             if (e != cudaSuccess) return cuda_fail(e);
             for (int r = -1; r < nb; ++r) {
                 const bool inject_here = (r == 0 && g_inject);
@@ -494,7 +507,7 @@ size_t workspace_bytes(int n) {
     const size_t npad = nb * kTB;
     const size_t base = kErrBytes + (2 * (size_t)kTB * npad + 2 * (size_t)kTB * kTB) * 4;
     const size_t panels2 = 2 * (size_t)kTB * npad * 4;       // second row/column panel buffers
-    const size_t flags = ((3 * nb + 3) * 4 + 255) / 256 * 256;  // flags + counters
+    const size_t flags = ((5 * nb + 4) * 4 + 255) / 256 * 256;  // flags, item counters, part counts
     return base + panels2 + flags;
 }
 }  // namespace apsp

@@ -70,13 +70,21 @@ enum : int { kCritNone = 0, kCritDiag = 1, kCritRow = 2, kCritCol = 3 };
 
 struct FusedItem {
     int kind, I, J, crit;
+    int s0, s1;  // a phase-3 item's k-slabs: [s0, s1) of the tile's TB / KS
 };
 
+// A phase-3 tile may be split into `split` items along k (fused_split in
+// fw_launch.h), so that a launch with few tiles still fills the GPU and a
+// critical tile finishes sooner.  The parts of a tile merge into D by the
+// same min-reduction, and min is associative, so the result does not depend
+// on the split.
+
 // Number of items of launch r (r = -1: prologue).
-__host__ __device__ inline long long fused_items(int r, int nb) {
+__host__ __device__ inline long long fused_items(int r, int nb, int split) {
     if (r < 0) return 1 + 2LL * (nb - 1);
-    if (r + 1 >= nb) return (long long)(nb - 1) * (nb - 1);
-    return (long long)nb * nb;
+    const long long p3 = (long long)(nb - 1) * (nb - 1) * split;
+    if (r + 1 >= nb) return p3;
+    return p3 + 1 + 2LL * (nb - 1);
 }
 
 // Ordinary phase-3 tiles taken before phase 2 of round r+1: enough work for
@@ -87,9 +95,11 @@ __host__ __device__ inline int fused_head(int nb, int grid) {
     return (int)(reg < want ? reg : want);
 }
 
-__device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x) {
+__device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x, int split) {
     FusedItem it;
     it.crit = kCritNone;
+    it.s0 = 0;
+    it.s1 = TB / KS;
     const int rn = r + 1;
     if (r < 0) {  // prologue: phase 1 and phase 2 of round 0
         if (l == 0) { it.kind = kItemP1; it.I = it.J = 0; return it; }
@@ -98,37 +108,45 @@ __device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x) {
         else { it.kind = kItemP2Col; it.I = q - (nb - 1) + 1; it.J = 0; }
         return it;
     }
+    const int per = (TB / KS) / split;  // slabs per part
+    it.kind = kItemP3;
     if (rn >= nb) {  // last round: phase 3 only
-        it.kind = kItemP3;
-        phase3_tile(l, nb - 1, r, it.I, it.J);
+        phase3_tile(l / split, nb - 1, r, it.I, it.J);
+        it.s0 = (l % split) * per;
+        it.s1 = it.s0 + per;
         return it;
     }
     const int c1 = 2 * nb - 3;
-    if (l < c1) {
-        it.kind = kItemP3;
-        if (l == 0) { it.I = it.J = rn; it.crit = kCritDiag; }
-        else if (l < nb - 1) { const int q = l - 1; it.I = rn; it.J = q + (q >= r ? 2 : 0); it.crit = kCritRow; }
-        else { const int q = l - (nb - 1); it.I = q + (q >= r ? 2 : 0); it.J = rn; it.crit = kCritCol; }
+    if (l < c1 * split) {  // the parts of one critical tile are consecutive
+        const int t = l / split;
+        it.s0 = (l % split) * per;
+        it.s1 = it.s0 + per;
+        if (t == 0) { it.I = it.J = rn; it.crit = kCritDiag; }
+        else if (t < nb - 1) { const int q = t - 1; it.I = rn; it.J = q + (q >= r ? 2 : 0); it.crit = kCritRow; }
+        else { const int q = t - (nb - 1); it.I = q + (q >= r ? 2 : 0); it.J = rn; it.crit = kCritCol; }
         return it;
     }
-    l -= c1;
+    l -= c1 * split;
     if (l == 0) { it.kind = kItemP1; it.I = it.J = rn; return it; }
     l -= 1;
     const int np2 = 2 * (nb - 1);
+    const int xi = x * split;
     int q;
-    if (l < x) {
+    if (l < xi) {
         q = l;
-    } else if (l < x + np2) {
-        const int p = l - x;
+    } else if (l < xi + np2) {
+        const int p = l - xi;
         if (p < nb - 1) { it.kind = kItemP2Row; it.I = rn; it.J = p + (p >= rn ? 1 : 0); }
         else { const int pp = p - (nb - 1); it.kind = kItemP2Col; it.I = pp + (pp >= rn ? 1 : 0); it.J = rn; }
         return it;
     } else {
         q = l - np2;
     }
-    it.kind = kItemP3;
     const int nb2 = nb > 2 ? nb - 2 : 1;  // ordinary tiles exist only when nb > 2
-    const int ti = q / nb2, tj = q - ti * nb2;
+    const int t = q / split;
+    it.s0 = (q % split) * per;
+    it.s1 = it.s0 + per;
+    const int ti = t / nb2, tj = t - ti * nb2;
     it.I = ti + (ti >= r ? 2 : 0);
     it.J = tj + (tj >= r ? 2 : 0);
     return it;
@@ -192,7 +210,7 @@ __device__ __forceinline__ void mask_outside(T (&acc)[8][8], const MMLayout& L, 
 
 template <typename T>
 __global__ void __launch_bounds__(FZ_THREADS, 1)
-fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, int nitems,
+fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, int nitems, int split,
                const __grid_constant__ FusedMaps maps, const FusedPtrs ptrs,
                unsigned long long timeout_ns, int inject) {
     extern __shared__ unsigned char fz_raw[];
@@ -256,13 +274,21 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             tma_reduce_min_2d(&maps.cmin, pw.J * TB, pw.I * TB, cdst);
             bulk_commit();
             if (pw.crit != kCritNone) {
+                // The tile is complete once all its parts have merged: the
+                // last part to finish sets the round flag and clears the
+                // count for the next launch.
                 bulk_wait_all();
+                const int c = pw.crit == kCritDiag ? 0 : pw.crit == kCritRow ? 1 + pw.J : 1 + nb + pw.I;
                 int* f = pw.crit == kCritDiag ? ptrs.flag_diag
                          : pw.crit == kCritRow ? ptrs.flag_row + pw.J
                                                : ptrs.flag_col + pw.I;
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __threadfence();
-                atomicExch(f, rn);
+                if (atomicAdd(ptrs.parts + c, 1) == split - 1) {
+                    atomicExch(ptrs.parts + c, 0);
+                    __threadfence();
+                    atomicExch(f, rn);
+                }
             } else {
                 bulk_wait_read_all();
             }
@@ -277,7 +303,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             w.kind = kItemP3;
             w.I = w.J = 0;
             w.crit = kCritNone;
-            if (!stop) w = fused_item(l, r, nb, x);
+            if (!stop) w = fused_item(l, r, nb, x, split);
             const bool merged = !stop && w.kind == kItemP3;
             // Phase 1 and 2 items need the C buffer and may wait for the
             // pending tile's flag: merge it first.  So does the end.
@@ -307,13 +333,13 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             }
             ++it;
             if (w.kind == kItemP1) continue;  // no slabs
-            for (int s = 0; s < TB / KS; ++s) {
+            for (int s = w.s0; s < w.s1; ++s) {
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (use > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1, err, timeout_ns)) {
                     ok = false;
                     break;
                 }
-                if (inject && l == 0 && s == 0) {
+                if (inject && l == 0 && s == w.s0) {
                     // Test hook: the first slab of item 0 (a phase-3 tile in
                     // every launch r >= 0) is never issued, so the consumers'
                     // bounded wait on it must run out (APSP_ETIMEOUT).
@@ -366,7 +392,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
         const int l = slots[it & 1];
         if (l < 0) return;
-        const FusedItem w = fused_item(l, r, nb, x);
+        const FusedItem w = fused_item(l, r, nb, x, split);
         const int row0 = w.I * TB, col0 = w.J * TB;
 
         if (w.kind == kItemP3) {
@@ -382,7 +408,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             for (int ri = 0; ri < 8; ++ri)
 #pragma unroll
                 for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::inf();
-            for (int s = 0; s < TB / KS; ++s, ++g) {
+            for (int s = w.s0; s < w.s1; ++s, ++g) {
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);

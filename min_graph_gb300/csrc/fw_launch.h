@@ -53,6 +53,7 @@ struct FusedPtrs {
     int* flag_row;    // [nb]
     int* flag_col;    // [nb]
     int* counters;    // [nb + 1]: item counter of launch r at index r + 1
+    int* parts;       // [2 nb + 1]: parts of each critical tile merged so far in this launch
     int* err;
 };
 
@@ -62,9 +63,16 @@ struct FusedArgs {
     int n, nb, npad, sms;
     unsigned long long timeout_ns;
     int inject;     // test hook: withhold one k-slab in this launch (forces a timeout)
+    int split;      // items per phase-3 tile along k: 1, 2 or 4
     FusedMaps maps;
     FusedPtrs ptrs;
 };
+
+// Items per phase-3 tile along k in the round-fused schedule (1, 2 or 4; it
+// divides the tile's four k-slabs).  A launch with fewer than four tiles per
+// SM splits its tiles by 4, so that it fills the GPU and each round's
+// critical tiles (on the path through phase 1 and phase 2) finish sooner.
+inline int fused_split(int nb, int sms) { return (long long)nb * nb < 4LL * sms ? 4 : 1; }
 
 // Opt the kernels into their shared-memory sizes on the current device.
 template <typename T> cudaError_t kernels_init();

@@ -32,11 +32,11 @@ cudaError_t kernels_init_impl() {
 
 template <typename T>
 cudaError_t launch_fused_impl(const FusedArgs& a, int r, cudaStream_t s) {
-    const long long items = fused_items(r, a.nb);
+    const long long items = fused_items(r, a.nb, a.split);
     if (items <= 0) return cudaSuccess;
     const int grid = (int)(items < a.sms ? items : a.sms);
     fw_round_fused<T><<<grid, FZ_THREADS, kFusedSmem, s>>>(static_cast<T*>(a.d), a.ld, a.n, r, a.nb,
-                                                           a.npad, (int)items, a.maps, a.ptrs,
+                                                           a.npad, (int)items, a.split, a.maps, a.ptrs,
                                                            a.timeout_ns, a.inject);
     return cudaGetLastError();
 }

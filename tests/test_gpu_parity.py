@@ -148,6 +148,22 @@ def test_workload_ba16384_full_matrix():
     assert_i32_exact(got, ref, "ba16384")
 
 
+@pytest.mark.parametrize("split", ["1", "4"])
+def test_tile_split_over_many_rounds(split, monkeypatch):
+    """A forced split on 32 rounds, where the head of ordinary tiles is
+    shorter than the ordinary tiles (so every item kind of a launch occurs):
+    sampled rows against Dijkstra, and both splits give the same matrix."""
+    monkeypatch.setenv("APSP_FUSED_SPLIT", split)
+    n = 4000
+    w = graphgen.er_i32(n, 0.01, 1, 1000, seed=41)
+    got, _ = gpu_solve(w)
+    src = np.random.default_rng(41).choice(n, 32, replace=False).astype(np.int32)
+    assert_i32_exact(got[src], oracle.dijkstra_i32(w, src), f"split {split} rows")
+    monkeypatch.setenv("APSP_FUSED_SPLIT", "2")
+    other, _ = gpu_solve(w)
+    assert np.array_equal(got, other)
+
+
 def test_workload_er32768_f32_sampled_rows():
     w = graphgen.make("er32768")
     got, _ = gpu_solve(w)
@@ -231,6 +247,9 @@ def test_empty_and_single():
 # Environment settings that select each schedule / phase-3 kernel.
 PHASE3_VARIANTS = [
     {},                                                # round-fused schedule (default)
+    {"APSP_FUSED_SPLIT": "1"},                         # ... each phase-3 tile one item
+    {"APSP_FUSED_SPLIT": "2"},                         # ... split in two along k
+    {"APSP_FUSED_SPLIT": "4"},                         # ... split in four along k
     {"APSP_FUSED": "0", "APSP_P3_COLS": "8"},          # three kernels, persistent phase 3
     {"APSP_FUSED": "0", "APSP_P3_COLS": "4"},          # ... with 512 consumer threads
     {"APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},     # ... with the cp.async phase 3
@@ -240,8 +259,8 @@ PHASE3_VARIANTS = [
 @pytest.mark.parametrize("n", [129, 255, 256, 300, 1000, 2100])
 def test_all_schedules_and_phase3_kernels_agree(n, monkeypatch):
     """Every schedule and phase-3 kernel gives the oracle's result: the
-    round-fused schedule, and the three-kernel schedule with each phase-3
-    kernel."""
+    round-fused schedule with each split of its phase-3 tiles along k, and
+    the three-kernel schedule with each phase-3 kernel."""
     w = graphgen.er_i32(n, 0.02, 1, 1000, seed=n + 7)
     ref = oracle.fw_i32(w, threads=threads())
     wf = graphgen.er_f32(n, 0.02, seed=n + 8)
@@ -258,9 +277,11 @@ def test_all_schedules_and_phase3_kernels_agree(n, monkeypatch):
 
 
 @pytest.mark.parametrize("fused", ["1", "0"])
-def test_bounded_wait_timeout_each_schedule(fused, monkeypatch):
-    """The timeout hook works in both schedules."""
+@pytest.mark.parametrize("split", ["1", "4"])
+def test_bounded_wait_timeout_each_schedule(fused, split, monkeypatch):
+    """The timeout hook works in both schedules (and both tile splits)."""
     monkeypatch.setenv("APSP_FUSED", fused)
+    monkeypatch.setenv("APSP_FUSED_SPLIT", split)
     w = graphgen.er_i32(600, 0.02, 1, 100, seed=13)
     t = torch.from_numpy(w).cuda()
     apsp.stream_check()
