@@ -65,7 +65,7 @@ constexpr int FZ_NAMED_BAR = 1;                 // consumer-only named barrier i
 // contract every entry is +0, a positive float or +inf (a -0.0 input is the
 // smallest pattern and acts as zero).
 
-enum : int { kItemP3 = 0, kItemP1 = 1, kItemP2Row = 2, kItemP2Col = 3 };
+enum : int { kItemP3 = 0, kItemP1 = 1, kItemP2Row = 2, kItemP2Col = 3, kItemFin = 4 };
 enum : int { kCritNone = 0, kCritDiag = 1, kCritRow = 2, kCritCol = 3 };
 
 struct FusedItem {
@@ -79,12 +79,15 @@ struct FusedItem {
 // same min-reduction, and min is associative, so the result does not depend
 // on the split.
 
-// Number of items of launch r (r = -1: prologue).
+// Number of items of launch r (r = -1: prologue).  Phase-2 tiles split
+// like phase-3 tiles; the finisher items that rewrite a split phase-2
+// tile's panel copy are handed out on top of these.
 __host__ __device__ inline long long fused_items(int r, int nb, int split) {
-    if (r < 0) return 1 + 2LL * (nb - 1);
+    const long long p2 = 2LL * (nb - 1) * split;
+    if (r < 0) return 1 + p2;
     const long long p3 = (long long)(nb - 1) * (nb - 1) * split;
     if (r + 1 >= nb) return p3;
-    return p3 + 1 + 2LL * (nb - 1);
+    return p3 + 1 + p2;
 }
 
 // Ordinary phase-3 tiles taken before phase 2 of round r+1: enough work for
@@ -101,14 +104,16 @@ __device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x, int
     it.s0 = 0;
     it.s1 = TB / KS;
     const int rn = r + 1;
+    const int per = (TB / KS) / split;  // slabs per part
     if (r < 0) {  // prologue: phase 1 and phase 2 of round 0
         if (l == 0) { it.kind = kItemP1; it.I = it.J = 0; return it; }
-        const int q = l - 1;
+        const int q = (l - 1) / split;
+        it.s0 = ((l - 1) % split) * per;
+        it.s1 = it.s0 + per;
         if (q < nb - 1) { it.kind = kItemP2Row; it.I = 0; it.J = q + 1; }
         else { it.kind = kItemP2Col; it.I = q - (nb - 1) + 1; it.J = 0; }
         return it;
     }
-    const int per = (TB / KS) / split;  // slabs per part
     it.kind = kItemP3;
     if (rn >= nb) {  // last round: phase 3 only
         phase3_tile(l / split, nb - 1, r, it.I, it.J);
@@ -129,13 +134,15 @@ __device__ __forceinline__ FusedItem fused_item(int l, int r, int nb, int x, int
     l -= c1 * split;
     if (l == 0) { it.kind = kItemP1; it.I = it.J = rn; return it; }
     l -= 1;
-    const int np2 = 2 * (nb - 1);
+    const int np2 = 2 * (nb - 1) * split;
     const int xi = x * split;
     int q;
     if (l < xi) {
         q = l;
-    } else if (l < xi + np2) {
-        const int p = l - xi;
+    } else if (l < xi + np2) {  // the parts of one phase-2 tile are consecutive
+        const int p = (l - xi) / split;
+        it.s0 = ((l - xi) % split) * per;
+        it.s1 = it.s0 + per;
         if (p < nb - 1) { it.kind = kItemP2Row; it.I = rn; it.J = p + (p >= rn ? 1 : 0); }
         else { const int pp = p - (nb - 1); it.kind = kItemP2Col; it.I = pp + (pp >= rn ? 1 : 0); it.J = rn; }
         return it;
@@ -264,6 +271,11 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         pw.I = pw.J = 0;
         pw.crit = kCritNone;
         uint32_t merges = 0;
+        // Split phase-2 tiles whose parts have all merged, waiting for their
+        // finisher item: code J for row tile (rn, J), nb + I for column tile
+        // (I, rn).  One merge per loop turn, so two entries suffice.
+        int fin[2] = {-1, -1};
+        int nfin = 0;
         // Merge the pending tile: D <- min(D, staged tile) by a TMA reduction
         // in L2.  A critical tile's flag is set once the reduction's writes
         // are complete; otherwise it is enough that the buffer has been read.
@@ -273,7 +285,18 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             if (!mbar_wait_bounded(bar_staged, merges & 1, err, timeout_ns)) return false;
             tma_reduce_min_2d(&maps.cmin, pw.J * TB, pw.I * TB, cdst);
             bulk_commit();
-            if (pw.crit != kCritNone) {
+            if (pw.kind != kItemP3) {
+                // A phase-2 part: once the tile's last part has merged, queue
+                // the finisher that rewrites the tile's panel copy.
+                bulk_wait_all();
+                const int c = pw.kind == kItemP2Row ? 1 + pw.J : 1 + nb + pw.I;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                if (atomicAdd(ptrs.parts + c, 1) == split - 1) {
+                    atomicExch(ptrs.parts + c, 0);
+                    fin[nfin++] = pw.kind == kItemP2Row ? pw.J : nb + pw.I;
+                }
+            } else if (pw.crit != kCritNone) {
                 // The tile is complete once all its parts have merged: the
                 // last part to finish sets the round flag and clears the
                 // count for the next launch.
@@ -297,18 +320,37 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             return true;
         };
         for (;;) {
-            const int l = atomicAdd(ptrs.counters + rn, 1);
-            const bool stop = l >= nitems;
             FusedItem w;
             w.kind = kItemP3;
             w.I = w.J = 0;
             w.crit = kCritNone;
-            if (!stop) w = fused_item(l, r, nb, x, split);
-            const bool merged = !stop && w.kind == kItemP3;
-            // Phase 1 and 2 items need the C buffer and may wait for the
-            // pending tile's flag: merge it first.  So does the end.
-            if (!merged) ok = merge_pending();
-            if (ok && !stop) {
+            w.s0 = 0;
+            w.s1 = TB / KS;
+            int l = -1;  // the item's index; the slot carries -2 - code for a finisher
+            bool stop = false;
+            if (nfin == 0) {
+                l = atomicAdd(ptrs.counters + rn, 1);
+                stop = l >= nitems;
+                if (!stop) w = fused_item(l, r, nb, x, split);
+            } else {
+                w.kind = kItemFin;
+            }
+            // Items merged through the C buffer: phase-3 tiles, and phase-2
+            // parts when tiles are split.
+            const bool merged = !stop && (w.kind == kItemP3 ||
+                                          (split > 1 && (w.kind == kItemP2Row || w.kind == kItemP2Col)));
+            // Everything but a phase-3 item needs the C buffer, and may wait
+            // for the pending tile's flag: merge it first.  So does the end.
+            if (w.kind != kItemP3 || stop) ok = merge_pending();
+            if (ok && stop && nfin > 0) continue;  // that merge completed a phase-2 tile: finish it first
+            if (w.kind == kItemFin) {
+                const int code = fin[0];
+                fin[0] = fin[1];
+                --nfin;
+                l = -2 - code;
+                w.I = code < nb ? rn : code - nb;
+                w.J = code < nb ? code : rn;
+            } else if (ok && !stop) {
                 if (w.kind == kItemP1 && r >= 0)
                     ok = flag_wait(ptrs.flag_diag, rn, err, timeout_ns);
                 else if (w.kind == kItemP2Row)
@@ -325,14 +367,18 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 break;
             }
             slots[it & 1] = l;
-            if (merged) {
+            if (w.kind == kItemP3) {
                 mbar_arrive(bar_cfull);  // no C tile: the consumers start from INF
             } else {
+                // phase 1, phase 2 (or its part) and finishers start from the
+                // D tile; a finisher's tile is complete (its parts' merges
+                // were waited for before they were counted)
+                if (w.kind == kItemFin) asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive_expect_tx(bar_cfull, FZ_C);
                 tma_load_2d(cdst, &maps.c, w.J * TB, w.I * TB, bar_cfull);
             }
             ++it;
-            if (w.kind == kItemP1) continue;  // no slabs
+            if (w.kind == kItemP1 || w.kind == kItemFin) continue;  // no slabs
             for (int s = w.s0; s < w.s1; ++s) {
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (use > 0 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1, err, timeout_ns)) {
@@ -362,8 +408,8 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             }
             if (!ok) break;
             if (merged) {
-                // this item's slabs are issued: merge the previous phase-3
-                // tile (its consumers are finishing it now)
+                // this item's slabs are issued: merge the previous tile (its
+                // consumers are finishing it now)
                 ok = merge_pending();
                 pw = w;
                 pend = true;
@@ -391,8 +437,19 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     for (int it = 0;; ++it) {
         if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
         const int l = slots[it & 1];
-        if (l < 0) return;
-        const FusedItem w = fused_item(l, r, nb, x, split);
+        if (l == -1) return;
+        FusedItem w;
+        if (l <= -2) {  // finisher of split phase-2 tile `code`
+            const int code = -2 - l;
+            w.kind = kItemFin;
+            w.I = code < nb ? rn : code - nb;
+            w.J = code < nb ? code : rn;
+            w.crit = kCritNone;
+            w.s0 = 0;
+            w.s1 = TB / KS;
+        } else {
+            w = fused_item(l, r, nb, x, split);
+        }
         const int row0 = w.I * TB, col0 = w.J * TB;
 
         if (w.kind == kItemP3) {
@@ -509,6 +566,35 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
 
         T acc[8][8];
         load_tile(acc, cbuf, L);
+
+        if (w.kind == kItemFin) {
+            // ------------- finisher: panel copy of a split phase-2 tile
+            // All parts have merged into D, so the tile loaded is final (and
+            // at most INF).  Write the copy that the next launch's phase 3
+            // reads: the row panel as is, the column panel transposed.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_cempty);
+            mask_outside(acc, L, row0, col0, n);
+            if (w.I == rn) {
+                T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
+#pragma unroll
+                for (int ri = 0; ri < 8; ++ri) {
+                    const int i = L.row(ri);
+                    vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                    vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                }
+            } else {
+                T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
+#pragma unroll
+                for (int ci = 0; ci < 8; ++ci) {
+                    const int k = L.col(ci);
+                    vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+                    vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+                }
+            }
+            continue;
+        }
+
         if (r <= 0) {  // from launch 1 on, every tile read was stored (clamped) by an earlier round
 #pragma unroll
             for (int ri = 0; ri < 8; ++ri)
@@ -530,7 +616,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             // the buffer is refilled by TMA later: order these writes first
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             consumer_barrier();
-            for (int s = 0; s < TB / KS; ++s, ++g) {
+            for (int s = w.s0; s < w.s1; ++s, ++g) {
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
@@ -540,20 +626,25 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_cempty);
-            T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
+            if (split > 1) {
+                consumer_barrier();  // every warp is done with the tile as B
+            } else {
+                T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
 #pragma unroll
-            for (int ri = 0; ri < 8; ++ri) {
-                const int i = L.row(ri);
-                gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
-                vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                for (int ri = 0; ri < 8; ++ri) {
+                    const int i = L.row(ri);
+                    gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                    gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                    vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                    vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                }
+                continue;
             }
         } else {
             // ----------------------------- phase 2, column panel tile (I, rn)
-            // A is the tile's transpose: the consumers write it into the A
-            // halves of the four ring stages this item uses, then run the
-            // product over B slabs (P).
+            // A is the tile's transpose: the consumers write it (the columns
+            // of this item's k-slabs) into the A halves of the ring stages
+            // this item uses, then run the product over B slabs (P).
             mask_outside(acc, L, row0, col0, n);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_cempty);
@@ -561,14 +652,17 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
 #pragma unroll
             for (int ci = 0; ci < 8; ++ci) {
                 const int k = L.col(ci);
-                T* Ast = reinterpret_cast<T*>(ring + ((g + k / KS) % FZ_STAGES) * FZ_STAGE) + (k % KS) * TB;
-                vstore4(Ast + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
-                vstore4(Ast + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+                const int sk = k / KS;
+                if (sk >= w.s0 && sk < w.s1) {
+                    T* Ast = reinterpret_cast<T*>(ring + ((g + sk - w.s0) % FZ_STAGES) * FZ_STAGE) + (k % KS) * TB;
+                    vstore4(Ast + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+                    vstore4(Ast + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+                }
             }
             // these stages are refilled by TMA later: order these writes first
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             consumer_barrier();
-            for (int s = 0; s < TB / KS; ++s, ++g) {
+            for (int s = w.s0; s < w.s1; ++s, ++g) {
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
@@ -576,20 +670,36 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * st);
             }
-            T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
+            if (split == 1) {
+                T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
 #pragma unroll
-            for (int ri = 0; ri < 8; ++ri) {
-                const int i = L.row(ri);
-                gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
-            }
+                for (int ri = 0; ri < 8; ++ri) {
+                    const int i = L.row(ri);
+                    gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+                    gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+                }
 #pragma unroll
-            for (int ci = 0; ci < 8; ++ci) {
-                const int k = L.col(ci);
-                vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
-                vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+                for (int ci = 0; ci < 8; ++ci) {
+                    const int k = L.col(ci);
+                    vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+                    vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+                }
+                continue;
             }
         }
+        // A part of a split phase-2 tile: stage it for the producer's merge
+        // into D (the panel copy is the finisher's job, once every part has
+        // merged).  Its accumulators started from the tile itself.
+        if (staged > 0 && !mbar_wait_bounded(bar_sfree, (staged - 1) & 1, err, timeout_ns)) return;
+#pragma unroll
+        for (int ri = 0; ri < 8; ++ri) {
+            vstore4(cbuf + L.row(ri) * TB + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+            vstore4(cbuf + L.row(ri) * TB + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_staged);
+        ++staged;
     }
 }
 
