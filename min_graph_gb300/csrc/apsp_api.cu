@@ -175,6 +175,13 @@ int fused_split_for(int nb, int sms) {
     return apsp::fused_split(nb, sms);
 }
 
+// APSP_FUSED_OVERLAP=0 launches each round only after the previous one has
+// ended (no programmatic dependent launch), for comparison and testing.
+bool fused_overlap_allowed() {
+    const char* v = std::getenv("APSP_FUSED_OVERLAP");
+    return !(v && std::strcmp(v, "0") == 0);
+}
+
 // APSP_P3_COLS=4|8 picks the persistent phase 3's accumulator columns per
 // thread (512 or 256 consumer threads); the default is kDefaultP3Cols.
 constexpr int kDefaultP3Cols = 8;
@@ -330,6 +337,7 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
         f.ptrs.counters = flags + 2 + 2 * nb;
         f.ptrs.parts = flags + 3 + 3 * nb;
         f.split = fused_split_for(nb, st.sms);
+        f.overlap = fused_overlap_allowed() ? 1 : 0;
         f.ptrs.err = a.err;
         const int ks = apsp::phase3_slab_rows();
         const unsigned long long pitch = (unsigned long long)npad * sizeof(T);

@@ -253,6 +253,11 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
         mbar_init_fence();
     }
     __syncthreads();
+    // A launch may start while the previous one drains (programmatic
+    // dependent launch): nothing in global memory is touched before the
+    // previous launch has completed and its writes are visible.  Without a
+    // programmatic predecessor this returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (tid >= FZ_CONSUMERS) {
         // ================================================== producer
@@ -332,6 +337,9 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 l = atomicAdd(ptrs.counters + rn, 1);
                 stop = l >= nitems;
                 if (!stop) w = fused_item(l, r, nb, x, split);
+                // this CTA takes no further items: the next launch may start
+                // on the SMs that drain
+                else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             } else {
                 w.kind = kItemFin;
             }

@@ -64,6 +64,7 @@ struct FusedArgs {
     unsigned long long timeout_ns;
     int inject;     // test hook: withhold one k-slab in this launch (forces a timeout)
     int split;      // items per phase-3 tile along k: 1, 2 or 4
+    int overlap;    // 1: launches r >= 0 may start while launch r - 1 drains (programmatic dependent launch)
     FusedMaps maps;
     FusedPtrs ptrs;
 };

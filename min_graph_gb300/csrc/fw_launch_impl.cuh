@@ -35,10 +35,21 @@ cudaError_t launch_fused_impl(const FusedArgs& a, int r, cudaStream_t s) {
     const long long items = fused_items(r, a.nb, a.split);
     if (items <= 0) return cudaSuccess;
     const int grid = (int)(items < a.sms ? items : a.sms);
-    fw_round_fused<T><<<grid, FZ_THREADS, kFusedSmem, s>>>(static_cast<T*>(a.d), a.ld, a.n, r, a.nb,
-                                                           a.npad, (int)items, a.split, a.maps, a.ptrs,
-                                                           a.timeout_ns, a.inject);
-    return cudaGetLastError();
+    // Launches after the prologue follow another launch of this kernel on the
+    // stream: let them start (barrier setup) while that one drains.  The
+    // kernel waits for its predecessor's completion before it reads memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(FZ_THREADS);
+    cfg.dynamicSmemBytes = kFusedSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (r >= 0 && a.overlap) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fw_round_fused<T>, static_cast<T*>(a.d), a.ld, a.n, r, a.nb, a.npad,
+                              (int)items, a.split, a.maps, a.ptrs, a.timeout_ns, a.inject);
 }
 
 template <typename T>

@@ -250,6 +250,7 @@ PHASE3_VARIANTS = [
     {"APSP_FUSED_SPLIT": "1"},                         # ... each phase-3 tile one item
     {"APSP_FUSED_SPLIT": "2"},                         # ... split in two along k
     {"APSP_FUSED_SPLIT": "4"},                         # ... split in four along k
+    {"APSP_FUSED_OVERLAP": "0"},                       # ... each launch after the previous ends
     {"APSP_FUSED": "0", "APSP_P3_COLS": "8"},          # three kernels, persistent phase 3
     {"APSP_FUSED": "0", "APSP_P3_COLS": "4"},          # ... with 512 consumer threads
     {"APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},     # ... with the cp.async phase 3
