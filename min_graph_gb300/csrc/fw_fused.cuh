@@ -239,6 +239,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     const int tid = threadIdx.x;
     const int rn = r + 1;
     const int x = fused_head(nb, gridDim.x);
+    const int per = (TB / KS) / split;  // k-slabs per phase-3 item
     int* err = ptrs.err;
 
     if (tid == 0) {
@@ -473,7 +474,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             for (int ri = 0; ri < 8; ++ri)
 #pragma unroll
                 for (int ci = 0; ci < 8; ++ci) acc[ri][ci] = Sem<T>::inf();
-            for (int s = w.s0; s < w.s1; ++s, ++g) {
+            for (int q = 0; q < per; ++q, ++g) {  // the item's k-slabs, in ring order
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
