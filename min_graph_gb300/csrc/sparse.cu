@@ -541,12 +541,18 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
 // CTA's shared memory (the Delta-stepping page's single-source setting).
 // The same buckets, light phases and heavy phase as above, with the state in
 // global memory:
-//   dist (the caller's output array), queued and wmin as in the CTA search,
-//   front (this phase's frontier) and rset (R) bitmaps.
+//   dist (the caller's output array), queued (the bucket structure, as in the
+//   CTA search), wmin (per bitmap word, the least distance of its queued
+//   vertices as of the last scan of the word), fresh (per word, the vertices
+//   whose distance a relaxation lowered since that scan) and rset (R).
 // Lane j of global warp g owns bitmap words (s * G + g) * 32 + j, s = 0, 1,
 // ... (G warps in the grid), so a warp's lanes hold 32 adjacent words.
-// Phases are separated by a grid barrier (below) that also reduces an OR
-// (is the bucket empty?) and a MIN (the next bucket) over all CTAs.  State
+// A light phase selects and relaxes in one sweep, and phases are separated
+// by one grid barrier (below) that also reduces an OR (did any warp select a
+// vertex?) and a MIN (the next bucket) over all CTAs.  Relaxations of other
+// warps run while a warp selects, so only the word's owner writes wmin, and
+// relaxations mark the word in fresh instead: a word may be skipped only
+// when it has no fresh vertex and its wmin is at least the bucket's end.  State
 // that other SMs write is read through L2 (ld.global.cg), never from a stale
 // L1 line.  Arc data is read-only and goes through the read-only path.  A
 // vertex with more than kGridBig arcs in the phase is not walked by its warp
@@ -580,7 +586,7 @@ struct GridArgs {
     int32_t* dist;
     uint32_t* queued;
     int32_t* wmin;
-    uint32_t* front;
+    uint32_t* fresh;
     uint32_t* rset;
     GridCtrl* ctrl;
     int4* big;       // grid-wide list of hub segments: (dv, begin, count, -)
@@ -592,30 +598,42 @@ struct GridArgs {
 __device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
 __device__ __forceinline__ int32_t ld_cg_i32(const int32_t* p) { return __ldcg(p); }
 
-// Grid barrier with an OR and a MIN reduction; slot k % 3 of the control
+// Grid barrier with a bitwise OR and a MIN reduction; slot k % 3 of the control
 // block holds barrier k's reductions, and CTA 0 clears slot (k + 2) % 3 once
 // past barrier k (every CTA has read that slot, used by barrier k - 1, and
 // none writes it before barrier k + 2).  Waits are bounded: after timeout_ns
-// the CTA sets ctrl->err; every waiting CTA sees it and leaves.  Returns
-// false when the search must stop.
+// the CTA sets ctrl->err; every waiting CTA sees it and leaves.  With
+// reset_list the last CTA to arrive empties the grid-wide hub list while all
+// the others wait, so no push of the next phase can precede the reset.
+// Returns false when the search must stop.
 __device__ bool grid_reduce(const GridArgs& a, int& k, int any_in, int32_t min_in, int& any_out,
-                            int32_t& min_out) {
-    __shared__ int s_min, s_any, s_err;
+                            int32_t& min_out, bool reset_list = false) {
+    __shared__ int s_min, s_any, s_err, s_or;
     const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0) s_min = INT_MAX;
-    const int any_b = __syncthreads_or(any_in);
+    if (tid == 0) {
+        s_min = INT_MAX;
+        s_or = 0;
+    }
+    __syncthreads();
+    const int wor = __reduce_or_sync(0xffffffffu, any_in);
     const int32_t wm = __reduce_min_sync(0xffffffffu, min_in);
+    if (lane == 0 && wor != 0) atomicOr(&s_or, wor);
     if (lane == 0 && wm != INT_MAX) atomicMin(&s_min, wm);
     __syncthreads();
     if (tid == 0) {
         GridCtrl* c = a.ctrl;
         const int slot = k % 3;
-        if (any_b) atomicOr(&c->any[slot], 1);
+        if (s_or) atomicOr(&c->any[slot], s_or);
         if (s_min != INT_MAX) atomicMin(&c->mn[slot], s_min);
         const unsigned g0 = *reinterpret_cast<volatile unsigned*>(&c->gen);
         __threadfence();
         const unsigned arrived = atomicAdd(&c->arrive, 1u) + 1u;
         if (arrived == gridDim.x) {
+            // every other CTA is waiting here, so shared state may be reset
+            if (reset_list) {
+                c->big_count = 0;
+                c->big_cursor = 0;
+            }
             atomicExch(&c->arrive, 0u);
             __threadfence();
             atomicAdd(&c->gen, 1u);
@@ -653,7 +671,7 @@ __device__ bool grid_reduce(const GridArgs& a, int& k, int any_in, int32_t min_i
 // Relax `cnt` arcs from `beg` for a vertex at distance dv, 32 lanes of a warp
 // striding over them, up to 4 loads in flight.
 __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int beg, int cnt, uint32_t dv,
-                                             int32_t* dist, uint32_t* queued, int32_t* wmin, int lane) {
+                                             int32_t* dist, uint32_t* queued, uint32_t* fresh, int lane) {
     int32_t best = INT_MAX;
     for (int o = 0; o < cnt; o += 128) {
         int2 x[4];
@@ -677,7 +695,7 @@ __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int 
             const int u = x[q].x;
             if (nd < du[q] && nd < atomicMin(dist + u, nd)) {
                 atomicOr(queued + (u >> 5), 1u << (u & 31));
-                atomicMin(wmin + (u >> 5), nd);
+                atomicOr(fresh + (u >> 5), 1u << (u & 31));
                 best = min(best, nd);
             }
         }
@@ -685,25 +703,17 @@ __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int 
     return best;
 }
 
-// Relax the light (kLight) or heavy arcs of every vertex in the bitmap `set`
-// (global), clearing it.  Batches of 32 vertices as in the CTA search; a
-// vertex with more than kGridBig arcs goes to the grid-wide list in segments
-// of kGridBig (its warp walks it itself if the list is full), and `pushed`
-// says whether this lane put any there.
+// Relax the light (kLight) or heavy arcs of the vertices of 32 bitmap words:
+// lane j holds in `bits` the members of word wbase + j (zero past the end),
+// and the whole warp takes part.  Batches of 32 vertices as in the CTA
+// search; a vertex with more than kGridBig arcs goes to the grid-wide list
+// in segments of kGridBig (its warp walks it itself if the list is full),
+// and `pushed` says whether this lane put any there.
 template <bool kLight>
-__device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
+__device__ int32_t expand_words(const GridArgs& a, long long wbase, uint32_t bits, int& pushed) {
+    const int lane = threadIdx.x & 31;
     int32_t best = INT_MAX;
-    for (int s = 0;; ++s) {
-        const long long wbase = ((long long)s * G + gw) * 32;
-        if (wbase >= a.nw) break;  // warp-uniform
-        const int i = (int)wbase + lane;
-        uint32_t bits = 0u;
-        if (i < a.nw) {
-            bits = ld_cg_u32(set + i);
-            if (bits) set[i] = 0u;
-        }
+    {
         const int c = __popc(bits);
         int wincl = c;
 #pragma unroll
@@ -747,7 +757,7 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
                 const int src = __ffs(hb) - 1;
                 best = min(best, relax_run(a.arcs, __shfl_sync(0xffffffffu, beg, src),
                                            __shfl_sync(0xffffffffu, cnt, src),
-                                           __shfl_sync(0xffffffffu, dv, src), a.dist, a.queued, a.wmin, lane));
+                                           __shfl_sync(0xffffffffu, dv, src), a.dist, a.queued, a.fresh, lane));
             }
             if (cnt > kGridBig) cnt = 0;
             int incl = cnt;
@@ -780,12 +790,32 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
                     const int u = x[q].x;
                     if (nd < du[q] && nd < atomicMin(a.dist + u, nd)) {
                         atomicOr(a.queued + (u >> 5), 1u << (u & 31));
-                        atomicMin(a.wmin + (u >> 5), nd);
+                        atomicOr(a.fresh + (u >> 5), 1u << (u & 31));
                         best = min(best, nd);
                     }
                 }
             }
         }
+    }
+    return best;
+}
+
+// The same for every vertex in the bitmap `set` (global), clearing it.
+template <bool kLight>
+__device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
+    int32_t best = INT_MAX;
+    for (int s = 0;; ++s) {
+        const long long wbase = ((long long)s * G + gw) * 32;
+        if (wbase >= a.nw) break;  // warp-uniform
+        const int i = (int)wbase + lane;
+        uint32_t bits = 0u;
+        if (i < a.nw) {
+            bits = ld_cg_u32(set + i);
+            if (bits) set[i] = 0u;
+        }
+        if (__any_sync(0xffffffffu, bits != 0u)) best = min(best, expand_words<kLight>(a, wbase, bits, pushed));
     }
     return best;
 }
@@ -803,30 +833,29 @@ __device__ int32_t drain_grid_list(const GridArgs& a) {
         idx = __shfl_sync(0xffffffffu, idx, 0);
         if (idx >= count) break;
         const int4 e = a.big[idx];
-        best = min(best, relax_run(a.arcs, e.y, e.z, (uint32_t)e.x, a.dist, a.queued, a.wmin, lane));
+        best = min(best, relax_run(a.arcs, e.y, e.z, (uint32_t)e.x, a.dist, a.queued, a.fresh, lane));
     }
     return best;
 }
 
 // The rest of a phase once its batches are done: the closing barrier, or,
 // when some warp put hub segments on the grid-wide list, a barrier, the
-// list shared out over the grid, and a second barrier.  CTA 0 empties the
-// list after that: the next push comes only after the next selection's
-// barrier.  `best` in: this lane's least successful relaxation; out: the
-// MIN over the grid.  Returns false when the search must stop.
-__device__ bool close_phase(const GridArgs& a, int& k, int pushed, int32_t in_min, int32_t& out_min) {
-    int any_big;
-    if (!grid_reduce(a, k, pushed, in_min, any_big, out_min)) return false;
-    if (!any_big) return true;
+// list shared out over the grid, and a second barrier whose last arriver
+// empties the list (the next phase may push as soon as it is past).
+// in_min: this lane's least successful relaxation; out_min: the MIN over
+// the grid.  flag_in / flag_out: one more OR over the grid, taken by the
+// same barrier.  Returns false when the search must stop.
+__device__ bool close_phase(const GridArgs& a, int& k, int pushed, int32_t in_min, int32_t& out_min,
+                            int flag_in = 0, int* flag_out = nullptr) {
+    int bits;
+    if (!grid_reduce(a, k, (pushed ? 1 : 0) | (flag_in ? 2 : 0), in_min, bits, out_min)) return false;
+    if (flag_out) *flag_out = bits >> 1;
+    if (!(bits & 1)) return true;
     const int32_t b = drain_grid_list(a);
     int unused;
     int32_t m2;
-    if (!grid_reduce(a, k, 0, b, unused, m2)) return false;
+    if (!grid_reduce(a, k, 0, b, unused, m2, true)) return false;  // its last arriver empties the list
     out_min = min(out_min, m2);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        a.ctrl->big_count = 0;
-        a.ctrl->big_cursor = 0;
-    }
     return true;
 }
 
@@ -841,63 +870,77 @@ __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) 
         const int32_t hi = hi_ll >= kUnreached ? kUnreached : (int32_t)hi_ll;
         int32_t beyond;
         for (;;) {  // light phases
+            // Each warp selects the queued vertices below hi in its bitmap
+            // words and relaxes their light arcs in the same sweep (a warp
+            // expands only the words it selected).  A word is looked at
+            // unless it has no fresh vertex and its wmin (exact as of its
+            // last scan) is at least hi; a look takes the fresh bits,
+            // computes the exact least distance of the vertices left
+            // queued, and clears only the bits it selected.  Anything a
+            // concurrent relaxation changes meanwhile is marked fresh again,
+            // for the next phase.  The phase in which no warp selects runs
+            // no relaxation, so its `beyond` (next bucket) is exact.
             beyond = INT_MAX;
-            int any = 0;
+            int any = 0, pushed = 0;
             for (int s = 0;; ++s) {
                 const long long wbase = ((long long)s * G + gw) * 32;
-                if (wbase >= a.nw) break;
+                if (wbase >= a.nw) break;  // warp-uniform
                 const int i = (int)wbase + lane;
-                if (i >= a.nw) continue;
-                const int32_t wm = ld_cg_i32(a.wmin + i);
-                if (wm >= hi) {
-                    beyond = min(beyond, wm);
-                    continue;
-                }
-                const uint32_t all = ld_cg_u32(a.queued + i);
                 uint32_t sel = 0u;
-                int32_t rem = INT_MAX;
-                const int vb = i * 32;
+                if (i < a.nw) {
+                    uint32_t fr = ld_cg_u32(a.fresh + i);
+                    if (fr) fr = atomicExch(a.fresh + i, 0u);
+                    const int32_t wm = ld_cg_i32(a.wmin + i);
+                    if (fr == 0u && wm >= hi) {
+                        beyond = min(beyond, wm);
+                    } else {
+                        // a relaxation sets the queued bit, then the fresh bit, and the
+                        // two may become visible in either order: a fresh bit taken
+                        // counts as queued (its distance is already in place, as the
+                        // relaxation's returning atomicMin on it came first)
+                        const uint32_t all = ld_cg_u32(a.queued + i) | fr;
+                        int32_t rem = INT_MAX;
+                        const int vb = i * 32;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {  // the word's distances, 4 at a time where any is queued
-                    const uint32_t nib = (all >> (q * 4)) & 0xFu;
-                    if (nib == 0u) continue;
-                    int32_t d4[4];
-                    if (vb + q * 4 + 3 < a.n) {
-                        const int4 v4 = __ldcg(reinterpret_cast<const int4*>(a.dist + vb + q * 4));
-                        d4[0] = v4.x;
-                        d4[1] = v4.y;
-                        d4[2] = v4.z;
-                        d4[3] = v4.w;
-                    } else {  // the ragged end of the array
+                        for (int q = 0; q < 8; ++q) {  // the word's distances, 4 at a time where any is queued
+                            const uint32_t nib = (all >> (q * 4)) & 0xFu;
+                            if (nib == 0u) continue;
+                            int32_t d4[4];
+                            if (vb + q * 4 + 3 < a.n) {
+                                const int4 v4 = __ldcg(reinterpret_cast<const int4*>(a.dist + vb + q * 4));
+                                d4[0] = v4.x;
+                                d4[1] = v4.y;
+                                d4[2] = v4.z;
+                                d4[3] = v4.w;
+                            } else {  // the ragged end of the array
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            d4[c] = vb + q * 4 + c < a.n ? ld_cg_i32(a.dist + vb + q * 4 + c) : INT_MAX;
-                    }
+                                for (int c = 0; c < 4; ++c)
+                                    d4[c] = vb + q * 4 + c < a.n ? ld_cg_i32(a.dist + vb + q * 4 + c) : INT_MAX;
+                            }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (!((nib >> c) & 1u)) continue;
-                        if (d4[c] < hi)
-                            sel |= 1u << (q * 4 + c);
-                        else
-                            rem = min(rem, d4[c]);
+                            for (int c = 0; c < 4; ++c) {
+                                if (!((nib >> c) & 1u)) continue;
+                                if (d4[c] < hi)
+                                    sel |= 1u << (q * 4 + c);
+                                else
+                                    rem = min(rem, d4[c]);
+                            }
+                        }
+                        if (sel) atomicAnd(a.queued + i, ~sel);
+                        if (rem != wm) a.wmin[i] = rem;  // only this lane writes word i's wmin
+                        beyond = min(beyond, rem);
+                        if (sel) {
+                            a.rset[i] = ld_cg_u32(a.rset + i) | sel;
+                            any = 1;
+                        }
                     }
                 }
-                a.queued[i] = all & ~sel;
-                a.wmin[i] = rem;
-                beyond = min(beyond, rem);
-                if (sel) {
-                    a.front[i] = sel;
-                    a.rset[i] = ld_cg_u32(a.rset + i) | sel;
-                    any = 1;
-                }
+                if (__any_sync(0xffffffffu, sel != 0u)) expand_words<true>(a, wbase, sel, pushed);
             }
-            int any_g;
             int32_t unused;
-            if (!grid_reduce(a, k, any, INT_MAX, any_g, unused)) return;
+            int any_g;
+            if (!close_phase(a, k, pushed, INT_MAX, unused, any, &any_g)) return;
             if (!any_g) break;
-            int pushed = 0;
-            expand_grid<true>(a, a.front, pushed);
-            if (!close_phase(a, k, pushed, INT_MAX, unused)) return;
         }
         int pushed = 0;
         const int32_t hbest = expand_grid<false>(a, a.rset, pushed);
@@ -917,7 +960,7 @@ __global__ void grid_init_kernel(GridArgs a, int src) {
     for (long long i = t; i < a.nw; i += stride) {
         a.queued[i] = i == (src >> 5) ? 1u << (src & 31) : 0u;
         a.wmin[i] = i == (src >> 5) ? 0 : INT_MAX;
-        a.front[i] = 0u;
+        a.fresh[i] = 0u;
         a.rset[i] = 0u;
     }
     if (t == 0) {
@@ -1282,7 +1325,7 @@ apsp_status_t build_csr(const int32_t* dist, int n, int ld, SparseState& st, lon
 }
 
 // Grid-search buffer: [ctrl 256 B | flags 256 B | (row_ptr copy) | nlight |
-// queued | wmin | front | rset | arcs | partition's big-vertex list | hub
+// queued | wmin | fresh | rset | arcs | partition's big-vertex list | hub
 // segment list], each section 256-byte aligned.  flags: [0..2] weight range,
 // [4] row_ptr check, [6] big-vertex count.  The segment list holds at most
 // one phase's hub segments: fewer than m / kGridBig full ones plus one
@@ -1317,7 +1360,7 @@ apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t*
     off += align256(nw * 4);
     a.wmin = reinterpret_cast<int32_t*>(buf + off);
     off += align256(nw * 4);
-    a.front = reinterpret_cast<uint32_t*>(buf + off);
+    a.fresh = reinterpret_cast<uint32_t*>(buf + off);
     off += align256(nw * 4);
     a.rset = reinterpret_cast<uint32_t*>(buf + off);
     off += align256(nw * 4);

@@ -253,6 +253,7 @@ PHASE3_VARIANTS = [
     {"APSP_FUSED_OVERLAP": "0"},                       # ... each launch after the previous ends
     {"APSP_FUSED": "0", "APSP_P3_COLS": "8"},          # three kernels, persistent phase 3
     {"APSP_FUSED": "0", "APSP_P3_COLS": "4"},          # ... with 512 consumer threads
+    {"APSP_FUSED": "0", "APSP_P3_STAGES": "5"},        # ... with a 5-stage slab ring
     {"APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},     # ... with the cp.async phase 3
 ]
 
