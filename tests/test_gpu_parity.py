@@ -175,6 +175,26 @@ def test_workload_er32768_f32_sampled_rows():
                      diag_rows=[(i, int(s)) for i, s in enumerate(src[:16])])
 
 
+def test_maximum_size_n65536_sampled_rows_and_columns():
+    """The largest size tested: n = 65536 (a 16 GiB int32 matrix, 512 tiles
+    per axis, so the most rounds and the longest flag and counter arrays),
+    on 16 seeded rows and 4 columns against Dijkstra."""
+    n = 65536
+    w = graphgen.er_i32(n, 8.0 / n, 1, 1000, seed=65536, threads=threads())
+    d = torch.from_numpy(w).cuda()
+    apsp.solve(d)
+    apsp.stream_check()
+    src = _sample(n, 16, 77)
+    idx = torch.from_numpy(src.astype(np.int64)).cuda()
+    got_rows = d.index_select(0, idx).cpu().numpy()
+    got_cols = d.index_select(1, idx[:4]).cpu().numpy().T
+    del d
+    torch.cuda.empty_cache()
+    assert_i32_exact(got_rows, oracle.dijkstra_i32(w, src, threads=threads()), "n=65536 rows")
+    assert_i32_exact(got_cols, oracle.dijkstra_i32(w, src[:4], reverse=True, threads=threads()),
+                     "n=65536 columns")
+
+
 # ---------------------------------------------------------------- API
 
 def test_host_entry_point_matches_device():
