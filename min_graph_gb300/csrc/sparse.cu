@@ -1158,15 +1158,18 @@ apsp_status_t partition_arcs(const int64_t* rp, const int32_t* col, const int32_
     return APSP_OK;
 }
 
-// Bucket width when the caller gives none: 3 * w_max / (mean out-degree),
-// so that with weights spread over [0, w_max] a vertex has about three light
-// arcs.  The Delta-stepping page tunes Delta by measurement (section 4.4);
-// the factor 3 was the fastest here on the Erdos-Renyi and Barabasi-Albert
-// workloads.
-int32_t default_delta(int n, long long m, int wmax) {
+// Bucket width when the caller gives none: factor * w_max / (mean
+// out-degree), so that with weights spread over [0, w_max] a vertex has about
+// `factor` light arcs.  The Delta-stepping page tunes Delta by measurement
+// (section 4.4).  Measured here: factor 3 was the fastest for the per-CTA
+// searches on the Erdos-Renyi and Barabasi-Albert workloads (kCtaDeltaFactor),
+// factor 2 for the grid-wide search on R-MAT scales 20-23 (kGridDeltaFactor).
+constexpr double kCtaDeltaFactor = 3.0;
+constexpr double kGridDeltaFactor = 2.0;
+int32_t default_delta(int n, long long m, int wmax, double factor = kCtaDeltaFactor) {
     if (m <= 0 || wmax <= 0) return 1;
     const double avg_deg = (double)m / (double)(n > 0 ? n : 1);
-    double d = 3.0 * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
+    double d = factor * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
     if (d < 1.0) d = 1.0;
     if (d > (double)kInf) d = (double)kInf;
     return (int32_t)d;
@@ -1384,7 +1387,7 @@ apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t*
     rc = weight_range(w, col, m, n, flags, s, &lo, &hi, &bad);
     if (rc != APSP_OK) return rc;
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
-    if (delta <= 0) delta = default_delta(n, m, hi);
+    if (delta <= 0) delta = default_delta(n, m, hi, kGridDeltaFactor);
     a.delta = delta;
     if (own_rp) {
         const cudaError_t e = cudaMemcpyAsync(rp_copy, rp, (size_t)(n + 1) * 8, cudaMemcpyDeviceToDevice, s);
