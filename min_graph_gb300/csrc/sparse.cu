@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <new>
@@ -1158,18 +1159,19 @@ apsp_status_t partition_arcs(const int64_t* rp, const int32_t* col, const int32_
     return APSP_OK;
 }
 
-// Bucket width when the caller gives none: factor * w_max / (mean
-// out-degree), so that with weights spread over [0, w_max] a vertex has about
-// `factor` light arcs.  The Delta-stepping page tunes Delta by measurement
-// (section 4.4).  Measured here: factor 3 was the fastest for the per-CTA
-// searches on the Erdos-Renyi and Barabasi-Albert workloads (kCtaDeltaFactor),
-// factor 2 for the grid-wide search on R-MAT scales 20-23 (kGridDeltaFactor).
-constexpr double kCtaDeltaFactor = 3.0;
-constexpr double kGridDeltaFactor = 2.0;
-int32_t default_delta(int n, long long m, int wmax, double factor = kCtaDeltaFactor) {
+// Bucket width when the caller gives none.  The Delta-stepping page tunes
+// Delta by measurement (section 4.4); these rules are fitted to sweeps here:
+//   per-CTA searches (Johnson): 0.8 * w_max / sqrt(mean out-degree).  Within
+//     a few percent of the best of 4-6 widths on er256, er2048, er8192 and
+//     ba16384, whose degrees run from 16 to 4096.
+//   grid-wide search: 2 * w_max / (mean out-degree).  Within 0.2 % of the
+//     best of six widths on R-MAT scales 20, 22 and 23.
+enum class DeltaRule { kCta, kGrid };
+int32_t default_delta(int n, long long m, int wmax, DeltaRule rule = DeltaRule::kCta) {
     if (m <= 0 || wmax <= 0) return 1;
-    const double avg_deg = (double)m / (double)(n > 0 ? n : 1);
-    double d = factor * (double)wmax / (avg_deg > 1.0 ? avg_deg : 1.0);
+    double avg_deg = (double)m / (double)(n > 0 ? n : 1);
+    if (avg_deg < 1.0) avg_deg = 1.0;
+    double d = rule == DeltaRule::kGrid ? 2.0 * (double)wmax / avg_deg : 0.8 * (double)wmax / sqrt(avg_deg);
     if (d < 1.0) d = 1.0;
     if (d > (double)kInf) d = (double)kInf;
     return (int32_t)d;
@@ -1387,7 +1389,7 @@ apsp_status_t grid_prepare(const int64_t* rp, const int32_t* col, const int32_t*
     rc = weight_range(w, col, m, n, flags, s, &lo, &hi, &bad);
     if (rc != APSP_OK) return rc;
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
-    if (delta <= 0) delta = default_delta(n, m, hi, kGridDeltaFactor);
+    if (delta <= 0) delta = default_delta(n, m, hi, DeltaRule::kGrid);
     a.delta = delta;
     if (own_rp) {
         const cudaError_t e = cudaMemcpyAsync(rp_copy, rp, (size_t)(n + 1) * 8, cudaMemcpyDeviceToDevice, s);
