@@ -629,7 +629,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
-                mm_core_fused<T, KS, 8>(acc, As, cbuf + s * KS * TB, L);
+                mm_core_fused<T, KS, 8, 1>(acc, As, cbuf + s * KS * TB, L);  // phase 2: not unrolled
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * st);
             }
@@ -675,7 +675,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
-                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
+                mm_core_fused<T, KS, 8, 1>(acc, As, As + KS * TB, L);  // phase 2: not unrolled
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * st);
             }
