@@ -296,7 +296,7 @@ fw_phase2_panels(T* __restrict__ D, long long ld, int n, int r, T* __restrict__ 
                 __syncthreads();
             }
         }
-        mm_core<T, Core<T>::value, P2_KH>(acc, As + kb * TB, Bs, L);
+        mm_core_fused<T, P2_KH, 8, 1>(acc, As + kb * TB, Bs, L);  // phase 2 runs the rolled core
     }
 
     if (is_row) {
