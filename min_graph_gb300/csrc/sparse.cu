@@ -870,6 +870,7 @@ __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) 
         const long long hi_ll = ((long long)(dmin / a.delta) + 1) * a.delta;
         const int32_t hi = hi_ll >= kUnreached ? kUnreached : (int32_t)hi_ll;
         int32_t beyond;
+        int32_t lmin = INT_MAX;  // least distance set by the last light phase, over the grid
         for (;;) {  // light phases
             // Each warp selects the queued vertices below hi in its bitmap
             // words and relaxes their light arcs in the same sweep (a warp
@@ -879,10 +880,17 @@ __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) 
             // computes the exact least distance of the vertices left
             // queued, and clears only the bits it selected.  Anything a
             // concurrent relaxation changes meanwhile is marked fresh again,
-            // for the next phase.  The phase in which no warp selects runs
-            // no relaxation, so its `beyond` (next bucket) is exact.
+            // for the next phase.
+            //   The bucket's light work is done once a phase sets no
+            // distance below hi: every vertex below hi queued before it was
+            // selected in it.  The next bucket then starts at the least of
+            // what the sweep left queued (`beyond`, per lane), what the
+            // phase's relaxations set (lmin; a relaxation after a word's
+            // look shows up there) and what the heavy phase sets: a lower
+            // bound on every queued distance, so nothing is left behind.
             beyond = INT_MAX;
             int any = 0, pushed = 0;
+            int32_t best = INT_MAX;
             for (int s = 0;; ++s) {
                 const long long wbase = ((long long)s * G + gw) * 32;
                 if (wbase >= a.nw) break;  // warp-uniform
@@ -936,17 +944,17 @@ __global__ void __launch_bounds__(kGridThreads, 2) sssp_grid_kernel(GridArgs a) 
                         }
                     }
                 }
-                if (__any_sync(0xffffffffu, sel != 0u)) expand_words<true>(a, wbase, sel, pushed);
+                if (__any_sync(0xffffffffu, sel != 0u))
+                    best = min(best, expand_words<true>(a, wbase, sel, pushed));
             }
-            int32_t unused;
             int any_g;
-            if (!close_phase(a, k, pushed, INT_MAX, unused, any, &any_g)) return;
-            if (!any_g) break;
+            if (!close_phase(a, k, pushed, best, lmin, any, &any_g)) return;
+            if (!any_g || lmin >= hi) break;
         }
         int pushed = 0;
         const int32_t hbest = expand_grid<false>(a, a.rset, pushed);
         int32_t next;
-        if (!close_phase(a, k, pushed, min(beyond, hbest), next)) return;
+        if (!close_phase(a, k, pushed, min(min(beyond, hbest), lmin), next)) return;
         if (next == INT_MAX) break;
         dmin = next;
     }
