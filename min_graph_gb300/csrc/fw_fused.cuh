@@ -5,20 +5,28 @@
 // Launch r runs, on one CTA per SM, the phase-3 tiles of round r together
 // with phase 1 and phase 2 of round r+1:
 //
-//   l in [0, c1)        phase 3 (round r): the tiles in row r+1 and column
+//   first               phase 3 (round r): the tiles in row r+1 and column
 //                       r+1 ("critical"; the diagonal (r+1, r+1) first)
-//   l = c1              phase 1 (round r+1): close tile (r+1, r+1)
-//   next x items        phase 3 (round r): ordinary tiles
-//   next 2(nb-1) items  phase 2 (round r+1): row panel (r+1, J), column
+//   then one item       phase 1 (round r+1): close tile (r+1, r+1)
+//   then x tiles        phase 3 (round r): ordinary tiles
+//   then 2(nb-1) tiles  phase 2 (round r+1): row panel (r+1, J), column
 //                       panel (I, r+1)
 //   the rest            phase 3 (round r): ordinary tiles
+// When a launch holds few tiles (fused_split), every phase-3 and phase-2
+// tile is split along k into `split` consecutive items of one or two
+// k-slabs; the parts merge into D by min-reduction, and the part that
+// completes a tile counts it done (a critical tile: its round flag; a
+// phase-2 tile: a finisher item, queued on the same CTA, that writes the
+// tile's panel copy for the next launch).
 //
 // CTAs take items in this order from a global counter.  Each item depends
 // only on items before it: phase 1 of r+1 on the critical tile (r+1, r+1),
 // and a phase-2 item on phase 1 of r+1 and on its own critical tile.  So
 // whichever CTAs are running always make progress, and no deadlock is
 // possible.  Waits on those dependencies are bounded spins on round-stamped
-// flags in global memory.  Phase 1 and phase 2 of round r+1 thus run inside
+// flags in global memory.  Launch r+1 may start on the SMs that launch r
+// frees (programmatic dependent launch) but touches no global memory before
+// launch r has completed.  Phase 1 and phase 2 of round r+1 thus run inside
 // round r's phase-3 work, instead of as two latency-bound launches between
 // rounds.  The row/column panel buffers alternate between rounds, so phase 2
 // of r+1 never overwrites what phase 3 of r is reading.  A prologue launch
@@ -36,6 +44,8 @@
 //                  A slabs <- transposed closed primary tile
 //   column panel:  C <- D tile; the consumers write its transpose into the
 //                  ring as the A operand; B slabs <- closed primary tile
+//                  (a phase-2 tile in one piece stores D and its panel copy
+//                  with plain stores; a part stages and merges like phase 3)
 //   phase 1:       C <- D tile; closed in registers with a published row and
 //                  column per step (as fw_phase1_diag)
 // A TMA load of a tile that crosses the edge of the matrix reads zeros
