@@ -101,6 +101,36 @@ apsp_status_t apsp_solve_host_i32(int32_t* host, int n, int ld, apsp_stream_t st
 apsp_status_t apsp_solve_host_f32(float* host, int n, int ld, apsp_stream_t stream);
 
 /*
+ * apsp_solve_host_batch_i32 / _f32 -- `count` independent n x n problems
+ * held in HOST memory, solved one after another with their copies
+ * overlapped.  Matrix b is uploaded from in[b] into one of two
+ * library-owned staging buffers on a library-owned copy stream, solved on
+ * `stream`, and its result is downloaded into out[b].  The upload of matrix
+ * b + 1 and the download of matrix b - 1 run while matrix b is solved, so
+ * with pinned host memory a batch takes about count solves plus one upload
+ * and one download.  The call returns when every result is in host memory.
+ *   in     host array of `count` pointers to the input matrices (leading
+ *          dimension ld).  Pointers may repeat: each input is only read.
+ *   out    host array of `count` pointers to the result matrices (leading
+ *          dimension ld).  out[b] may equal in[b] (in place).  It must not
+ *          overlap any other in[] or out[] matrix.
+ *   count  number of problems, >= 0 (0: no-op, APSP_OK).
+ *   n, ld  as for apsp_solve; the same for every problem.
+ * Ownership: the caller keeps every host buffer; the library keeps the
+ * staging buffers, the copy stream and its events until apsp_release().
+ * Errors: APSP_EINVAL for count < 0, a bad n or ld, or a NULL pointer among
+ * in[0..count) and out[0..count) (checked before any work); APSP_ECUDA for a
+ * failed copy or launch; APSP_ENOMEM when a staging buffer cannot be
+ * allocated.  After an error no further problem is started, and the call
+ * still waits for the work already enqueued.  Device-side wait timeouts are
+ * reported by apsp_stream_check(stream), as for apsp_solve.
+ */
+apsp_status_t apsp_solve_host_batch_i32(const int32_t* const* in, int32_t* const* out, int count, int n,
+                                        int ld, apsp_stream_t stream);
+apsp_status_t apsp_solve_host_batch_f32(const float* const* in, float* const* out, int count, int n, int ld,
+                                        apsp_stream_t stream);
+
+/*
  * apsp_validate_i32 / _f32 -- check the preconditions on the device.
  *   flags_dev  device pointer to one int.  The call ORs bits into it and does
  *              not clear it first:

@@ -68,6 +68,10 @@ def load():
             f = getattr(lib, name)
             f.argtypes = [vp, i32, i32, vp]
             f.restype = i32
+        for name in ("apsp_solve_host_batch_i32", "apsp_solve_host_batch_f32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, i32, i32, i32, vp]
+            f.restype = i32
         for name in ("apsp_validate_i32", "apsp_validate_f32"):
             f = getattr(lib, name)
             f.argtypes = [vp, i32, i32, vp, vp]
@@ -214,6 +218,54 @@ def solve_host(a, n: int | None = None, ld: int | None = None, stream=None):
     else:
         raise TypeError("dtype must be int32 or float32")
     return a
+
+
+def _host_matrix(a):
+    """(pointer, rows, cols, ld, dtype name) of a row-major 2-D host matrix
+    (numpy array or CPU tensor)."""
+    import numpy as np
+    import torch
+
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda or a.dim() != 2 or (a.shape[0] > 1 and a.stride(1) != 1):
+            raise ValueError("expected a row-major 2-D CPU tensor")
+        dt = {torch.int32: "i32", torch.float32: "f32"}.get(a.dtype)
+        return a.data_ptr(), a.shape[0], a.shape[1], a.stride(0), dt
+    if not isinstance(a, np.ndarray) or a.ndim != 2 or not a.flags.c_contiguous:
+        raise ValueError("expected a C-contiguous 2-D numpy array")
+    dt = {np.dtype(np.int32): "i32", np.dtype(np.float32): "f32"}.get(a.dtype)
+    return a.ctypes.data, a.shape[0], a.shape[1], a.shape[1], dt
+
+
+def solve_host_batch(inputs, outputs=None, stream=None):
+    """Solve several square HOST matrices of one size and dtype (numpy arrays
+    or CPU tensors, ideally pinned) with their copies overlapped
+    (apsp_solve_host_batch_*): while problem b is solved, problem b + 1 is
+    uploaded and problem b - 1 downloaded.  Results go to `outputs` (default:
+    in place; an input may appear several times only with distinct outputs).
+    Blocking; uses the current CUDA device.  Returns the outputs."""
+    inputs = list(inputs)
+    outputs = inputs if outputs is None else list(outputs)
+    if len(outputs) != len(inputs):
+        raise ValueError("inputs and outputs differ in length")
+    lib = load()
+    if not inputs:
+        return outputs
+    ins = [_host_matrix(a) for a in inputs]
+    outs = [_host_matrix(a) for a in outputs]
+    _, n, cols, ld, dt = ins[0]
+    for (_, r, c, l, d) in ins + outs:
+        if r != n or c != n or l != ld or d != dt:
+            raise ValueError("every matrix must be square with the same size, leading dimension and dtype")
+    if dt is None:
+        raise TypeError("dtype must be int32 or float32")
+    count = len(ins)
+    in_arr = (ctypes.c_void_p * count)(*[x[0] for x in ins])
+    out_arr = (ctypes.c_void_p * count)(*[x[0] for x in outs])
+    s = 0 if stream is None else (int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+    name = "apsp_solve_host_batch_" + dt
+    _check(getattr(lib, name)(in_arr, out_arr, count, n, ld, s), name)
+    return outputs
 
 
 def solve_ooc(a, device_bytes: int = 0, block: int = 0, stream=None):

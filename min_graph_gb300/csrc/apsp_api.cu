@@ -43,6 +43,10 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void* stage = nullptr;       // staging matrix for the host-buffer entry points
     size_t stage_bytes = 0;
+    void* stage2 = nullptr;      // second staging matrix (batched host solves)
+    size_t stage2_bytes = 0;
+    cudaStream_t copy = nullptr; // copy stream of the batched host solves
+    cudaEvent_t bev[5] = {};     // their events: start, uploaded[2], solved[2]
     cudaEvent_t done = nullptr;  // end of the last solve that used ws
 };
 
@@ -455,6 +459,69 @@ apsp_status_t solve_host(T* h, int n, int ld, cudaStream_t s) {
     return APSP_OK;
 }
 
+// Batched host solves: matrix b is uploaded into staging buffer b % 2 on a
+// copy stream, solved on s, and downloaded on the copy stream, so the copies
+// of matrices b - 1 and b + 1 overlap the solve of matrix b.  On the copy
+// stream, the upload of matrix b + 2 follows the download of matrix b, which
+// used the same buffer; the solve of matrix b waits for its upload.
+template <typename T>
+apsp_status_t solve_host_batch(const T* const* in, T* const* out, int count, int n, int ld, cudaStream_t s) {
+    if (count < 0 || n < 0 || n > APSP_MAX_N || ld < n) return APSP_EINVAL;
+    if (count == 0 || n == 0) return APSP_OK;
+    if (in == nullptr || out == nullptr) return APSP_EINVAL;
+    for (int b = 0; b < count; ++b)
+        if (in[b] == nullptr || out[b] == nullptr) return APSP_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    apsp_status_t rc = device_state(&st);
+    if (rc != APSP_OK) return rc;
+    const int ldd = (n + 3) & ~3;  // vector-friendly device pitch
+    const size_t bytes = (size_t)n * ldd * sizeof(T);
+    rc = ensure_buffer(*st, &st->stage, &st->stage_bytes, bytes);
+    if (rc == APSP_OK && count > 1) rc = ensure_buffer(*st, &st->stage2, &st->stage2_bytes, bytes);
+    if (rc != APSP_OK) return rc;
+    cudaError_t e = cudaSuccess;
+    if (!st->copy) e = cudaStreamCreateWithFlags(&st->copy, cudaStreamNonBlocking);
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+        if (!st->bev[i]) e = cudaEventCreateWithFlags(&st->bev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e);
+    T* buf[2] = {static_cast<T*>(st->stage), static_cast<T*>(st->stage2)};
+    cudaStream_t c = st->copy;
+    auto copy = [&](T* dst, size_t dpitch, const T* src, size_t spitch, cudaMemcpyKind kind) {
+        if (dpitch == spitch) return cudaMemcpyAsync(dst, src, (size_t)n * dpitch * sizeof(T), kind, c);
+        return cudaMemcpy2DAsync(dst, dpitch * sizeof(T), src, spitch * sizeof(T), (size_t)n * sizeof(T), n,
+                                 kind, c);
+    };
+    auto upload = [&](int b) {
+        cudaError_t x = copy(buf[b & 1], ldd, in[b], ld, cudaMemcpyHostToDevice);
+        if (x == cudaSuccess) x = cudaEventRecord(st->bev[1 + (b & 1)], c);
+        return x;
+    };
+    // the staging buffers may still be in use by earlier work on s
+    e = cudaEventRecord(st->bev[0], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c, st->bev[0], 0);
+    if (e == cudaSuccess) e = upload(0);
+    if (e == cudaSuccess && count > 1) e = upload(1);
+    for (int b = 0; b < count && e == cudaSuccess; ++b) {
+        const int k = b & 1;
+        e = cudaStreamWaitEvent(s, st->bev[1 + k], 0);
+        if (e != cudaSuccess) break;
+        rc = solve_locked<T>(buf[k], n, ldd, s, *st);
+        if (rc != APSP_OK) break;
+        e = cudaEventRecord(st->bev[3 + k], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c, st->bev[3 + k], 0);
+        if (e == cudaSuccess) e = copy(out[b], ld, buf[k], ldd, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess && b + 2 < count) e = upload(b + 2);
+    }
+    // wait for everything enqueued, even after an error
+    const cudaError_t e1 = cudaStreamSynchronize(c);
+    const cudaError_t e2 = cudaStreamSynchronize(s);
+    if (rc != APSP_OK) return rc;
+    if (e == cudaSuccess) e = e1 != cudaSuccess ? e1 : e2;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return APSP_OK;
+}
+
 // ------------------------------------------------------------- validator
 
 template <typename T>
@@ -542,6 +609,16 @@ apsp_status_t apsp_solve_host_f32(float* host, int n, int ld, apsp_stream_t stre
     return solve_host<float>(host, n, ld, (cudaStream_t)stream);
 }
 
+apsp_status_t apsp_solve_host_batch_i32(const int32_t* const* in, int32_t* const* out, int count, int n,
+                                        int ld, apsp_stream_t stream) {
+    return solve_host_batch<int32_t>(in, out, count, n, ld, (cudaStream_t)stream);
+}
+
+apsp_status_t apsp_solve_host_batch_f32(const float* const* in, float* const* out, int count, int n, int ld,
+                                        apsp_stream_t stream) {
+    return solve_host_batch<float>(in, out, count, n, ld, (cudaStream_t)stream);
+}
+
 apsp_status_t apsp_validate_i32(const int32_t* dist, int n, int ld, apsp_stream_t stream,
                                 int* flags_dev) {
     return validate<int32_t>(dist, n, ld, (cudaStream_t)stream, flags_dev);
@@ -598,14 +675,22 @@ apsp_status_t apsp_release(void) {
     apsp_status_t rc = APSP_OK;
     for (size_t dev = 0; dev < g_dev.size(); ++dev) {
         DeviceState& st = g_dev[dev];
-        if (!st.ws && !st.stage && !st.done) continue;
+        if (!st.ws && !st.stage && !st.stage2 && !st.copy && !st.done) continue;
         if (cudaSetDevice((int)dev) != cudaSuccess) { rc = APSP_ECUDA; continue; }
         if (st.done) cudaEventSynchronize(st.done);
+        if (st.copy) cudaStreamSynchronize(st.copy);
         if (st.ws) cudaFree(st.ws);
         if (st.stage) cudaFree(st.stage);
+        if (st.stage2) cudaFree(st.stage2);
         if (st.done) cudaEventDestroy(st.done);
-        st.ws = st.stage = nullptr;
-        st.ws_bytes = st.stage_bytes = 0;
+        for (cudaEvent_t& ev : st.bev) {
+            if (ev) cudaEventDestroy(ev);
+            ev = nullptr;
+        }
+        if (st.copy) cudaStreamDestroy(st.copy);
+        st.ws = st.stage = st.stage2 = nullptr;
+        st.ws_bytes = st.stage_bytes = st.stage2_bytes = 0;
+        st.copy = nullptr;
         st.done = nullptr;
     }
     cudaSetDevice(cur);

@@ -68,6 +68,19 @@ def test_bad_arguments_rejected_without_cuda(libs):
     for fn in (lib.apsp_validate_i32, lib.apsp_validate_f32):
         assert fn(fake, 4, 4, None, None) == apsp.EINVAL    # no flags pointer
         assert fn(fake, 4, 3, None, fake) == apsp.EINVAL
+    arr = (ctypes.c_void_p * 2)(fake, fake)
+    nul = (ctypes.c_void_p * 2)(fake, None)
+    for fn in (lib.apsp_solve_host_batch_i32, lib.apsp_solve_host_batch_f32):
+        assert fn(arr, arr, -1, 5, 5, None) == apsp.EINVAL    # count < 0
+        assert fn(arr, arr, 2, -1, 5, None) == apsp.EINVAL    # n < 0
+        assert fn(arr, arr, 2, 6, 5, None) == apsp.EINVAL     # ld < n
+        assert fn(arr, arr, 2, apsp.MAX_N + 1, apsp.MAX_N + 1, None) == apsp.EINVAL
+        assert fn(None, arr, 2, 5, 5, None) == apsp.EINVAL    # no input array
+        assert fn(arr, None, 2, 5, 5, None) == apsp.EINVAL    # no output array
+        assert fn(nul, arr, 2, 5, 5, None) == apsp.EINVAL     # a NULL input
+        assert fn(arr, nul, 2, 5, 5, None) == apsp.EINVAL     # a NULL output
+        assert fn(None, None, 0, 5, 5, None) == apsp.OK       # count = 0 is a no-op
+        assert fn(nul, nul, 2, 0, 0, None) == apsp.OK         # so is n = 0
     assert lib.apsp_phase_timing_enable(0) == apsp.OK
     assert lib.apsp_debug_inject_phase3_timeout(0) == apsp.EINVAL
     assert lib.apsp_debug_inject_phase3_timeout(3 * 10**9) == apsp.EINVAL

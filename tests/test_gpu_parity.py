@@ -211,6 +211,40 @@ def test_host_entry_point_matches_device():
         assert_f32_close(pinned.numpy(), oracle.fw_f64(wf, threads=threads()), f"host f32 n={n}")
 
 
+def test_host_batch_matches_oracle():
+    # four different problems, one of them twice (inputs may repeat when the
+    # outputs differ), a ragged leading dimension with canaries, int32 and fp32
+    n, ld = 777, 781
+    ws = [graphgen.er_i32(n, p, 1, 100, seed=s) for s, p in ((11, 0.01), (12, 0.05), (13, 0.3))]
+    ins = []
+    for w in ws + [ws[0]]:
+        buf = torch.full((n, ld), -3, dtype=torch.int32).pin_memory()
+        buf[:, :n] = torch.from_numpy(w)
+        ins.append(buf)
+    outs = [torch.full((n, ld), -5, dtype=torch.int32).pin_memory() for _ in ins]
+    outs[1] = ins[1]  # one result in place
+    apsp.solve_host_batch([x[:, :n] for x in ins], [x[:, :n] for x in outs])  # views: ld > n
+    refs = [oracle.fw_i32(w, threads=threads()) for w in ws]
+    for b, ref in enumerate(refs + [refs[0]]):
+        assert_i32_exact(outs[b][:, :n].numpy(), ref, f"batch problem {b}")
+    assert np.all(ins[0][:, :n].numpy() == ws[0])  # inputs only read
+    for b in (0, 2, 3):
+        assert np.all(outs[b][:, n:].numpy() == -5)
+    assert np.all(ins[1][:, n:].numpy() == -3)
+    # fp32, in place, odd count, unpinned numpy arrays
+    wf = [graphgen.er_f32(300, 0.05, seed=s) for s in (21, 22, 23)]
+    bufs = [w.copy() for w in wf]
+    apsp.solve_host_batch(bufs)
+    for b, w in enumerate(wf):
+        assert_f32_close(bufs[b], oracle.fw_f64(w, threads=threads()), f"batch f32 problem {b}")
+    # one problem, and none
+    one = [graphgen.er_i32(129, 0.1, 1, 50, seed=31)]
+    ref = oracle.fw_i32(one[0], threads=threads())
+    apsp.solve_host_batch(one)
+    assert_i32_exact(one[0], ref, "batch of one")
+    assert apsp.solve_host_batch([]) == []
+
+
 def test_validator_flags():
     w = graphgen.er_i32(300, 0.05, 1, 100, seed=1)
     t = torch.from_numpy(w).cuda()
