@@ -354,9 +354,14 @@ apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st)
             ok = encode_2d(&f.maps.cmin, false, d, n, n, (unsigned long long)ld * sizeof(T), kTB, kTB);
         else
             f.maps.cmin = a.tm_c;
+        // The panels in the layout apsp::kPanelPack<T> names: pk = 2 views a
+        // TB x npad panel as TB / 2 rows of 2 npad, k-pair interleaved.
+        const int pk = apsp::kPanelPack<T>;
         for (int b = 0; b < 2; ++b) {
-            ok = ok && encode_2d(&f.maps.rowp[b], is_float, f.ptrs.rowp[b], npad, kTB, pitch, kTB, ks);
-            ok = ok && encode_2d(&f.maps.colpT[b], is_float, f.ptrs.colpT[b], npad, kTB, pitch, kTB, ks);
+            ok = ok && encode_2d(&f.maps.rowp[b], is_float, f.ptrs.rowp[b], (unsigned long long)npad * pk,
+                                 kTB / pk, pitch * pk, kTB * pk, ks / pk);
+            ok = ok && encode_2d(&f.maps.colpT[b], is_float, f.ptrs.colpT[b], (unsigned long long)npad * pk,
+                                 kTB / pk, pitch * pk, kTB * pk, ks / pk);
         }
         ok = ok && encode_2d(&f.maps.prim, is_float, a.prim, kTB, kTB, kTB * sizeof(T), kTB, ks);
         ok = ok && encode_2d(&f.maps.primT, is_float, a.primT, kTB, kTB, kTB * sizeof(T), kTB, ks);

@@ -225,6 +225,57 @@ __device__ __forceinline__ void mask_outside(T (&acc)[8][8], const MMLayout& L, 
             if (row0 + L.row(ri) >= n || col0 + L.col(ci) >= n) acc[ri][ci] = Sem<T>::inf();
 }
 
+// The workspace copy of this thread's 8 x 8 block of row-panel tile (rn, J)
+// (tile row i is panel row k = i), in the layout kPanelPack<T> names.
+template <typename T>
+__device__ __forceinline__ void store_row_panel(T* rp, const T (&acc)[8][8], const MMLayout& L, int col0,
+                                                int npad) {
+    if constexpr (kPanelPack<T> == 1) {
+#pragma unroll
+        for (int ri = 0; ri < 8; ++ri) {
+            const int i = L.row(ri);
+            vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
+            vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
+        }
+    } else {
+        // rows i and i + 1 (i even) form one k-pair row of the panel
+#pragma unroll
+        for (int ri = 0; ri < 8; ri += 2) {
+            T* p = rp + (long long)(L.row(ri) >> 1) * (2 * npad) + 2 * col0;
+            vstore4(p + 2 * L.cB0, acc[ri][0], acc[ri + 1][0], acc[ri][1], acc[ri + 1][1]);
+            vstore4(p + 2 * L.cB0 + 4, acc[ri][2], acc[ri + 1][2], acc[ri][3], acc[ri + 1][3]);
+            vstore4(p + 2 * L.cB1, acc[ri][4], acc[ri + 1][4], acc[ri][5], acc[ri + 1][5]);
+            vstore4(p + 2 * L.cB1 + 4, acc[ri][6], acc[ri + 1][6], acc[ri][7], acc[ri + 1][7]);
+        }
+    }
+}
+
+// The workspace copy, transposed, of this thread's block of column-panel
+// tile (I, rn) (tile column k is panel row k), in the layout kPanelPack<T>
+// names.
+template <typename T>
+__device__ __forceinline__ void store_col_panel(T* cp, const T (&acc)[8][8], const MMLayout& L, int row0,
+                                                int npad) {
+    if constexpr (kPanelPack<T> == 1) {
+#pragma unroll
+        for (int ci = 0; ci < 8; ++ci) {
+            const int k = L.col(ci);
+            vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
+            vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
+        }
+    } else {
+        // columns k and k + 1 (k even) form one k-pair row of the panel
+#pragma unroll
+        for (int ci = 0; ci < 8; ci += 2) {
+            T* p = cp + (long long)(L.col(ci) >> 1) * (2 * npad) + 2 * row0;
+            vstore4(p + 2 * L.rA0, acc[0][ci], acc[0][ci + 1], acc[1][ci], acc[1][ci + 1]);
+            vstore4(p + 2 * L.rA0 + 4, acc[2][ci], acc[2][ci + 1], acc[3][ci], acc[3][ci + 1]);
+            vstore4(p + 2 * L.rA1, acc[4][ci], acc[4][ci + 1], acc[5][ci], acc[5][ci + 1]);
+            vstore4(p + 2 * L.rA1 + 4, acc[6][ci], acc[6][ci + 1], acc[7][ci], acc[7][ci + 1]);
+        }
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(FZ_THREADS, 1)
 fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, int nitems, int split,
@@ -413,9 +464,10 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 }
                 const uint32_t dst = rdst + st * FZ_STAGE;
                 if (w.kind == kItemP3) {
+                    constexpr int PK = kPanelPack<T>;  // panels k-pair interleaved when 2
                     mbar_arrive_expect_tx(bar_full + 8 * st, FZ_STAGE);
-                    tma_load_2d(dst, &maps.colpT[pb], w.I * TB, s * KS, bar_full + 8 * st);
-                    tma_load_2d(dst + FZ_SLAB, &maps.rowp[pb], w.J * TB, s * KS, bar_full + 8 * st);
+                    tma_load_2d(dst, &maps.colpT[pb], w.I * TB * PK, s * (KS / PK), bar_full + 8 * st);
+                    tma_load_2d(dst + FZ_SLAB, &maps.rowp[pb], w.J * TB * PK, s * (KS / PK), bar_full + 8 * st);
                 } else if (w.kind == kItemP2Row) {
                     mbar_arrive_expect_tx(bar_full + 8 * st, FZ_SLAB);
                     tma_load_2d(dst, &maps.primT, 0, s * KS, bar_full + 8 * st);
@@ -488,7 +540,10 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 const uint32_t st = g % FZ_STAGES, use = g / FZ_STAGES;
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
-                mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
+                if constexpr (kPanelPack<T> == 2)
+                    mm_core<T, kCorePacked, KS>(acc, As, As + KS * TB, L);  // k-pair interleaved slabs
+                else
+                    mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * st);
             }
@@ -594,23 +649,10 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_cempty);
             mask_outside(acc, L, row0, col0, n);
-            if (w.I == rn) {
-                T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
-#pragma unroll
-                for (int ri = 0; ri < 8; ++ri) {
-                    const int i = L.row(ri);
-                    vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                    vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
-                }
-            } else {
-                T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
-#pragma unroll
-                for (int ci = 0; ci < 8; ++ci) {
-                    const int k = L.col(ci);
-                    vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
-                    vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
-                }
-            }
+            if (w.I == rn)
+                store_row_panel(static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]), acc, L, col0, npad);
+            else
+                store_col_panel(static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]), acc, L, row0, npad);
             continue;
         }
 
@@ -648,15 +690,13 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             if (split > 1) {
                 consumer_barrier();  // every warp is done with the tile as B
             } else {
-                T* rp = static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]);
 #pragma unroll
                 for (int ri = 0; ri < 8; ++ri) {
                     const int i = L.row(ri);
                     gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
                     gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
-                    vstore4(rp + (long long)i * npad + col0 + L.cB0, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
-                    vstore4(rp + (long long)i * npad + col0 + L.cB1, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
                 }
+                store_row_panel(static_cast<T*>(nbuf ? ptrs.rowp[1] : ptrs.rowp[0]), acc, L, col0, npad);
                 continue;
             }
         } else {
@@ -690,19 +730,13 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 if (lane == 0) mbar_arrive(bar_empty + 8 * st);
             }
             if (split == 1) {
-                T* cp = static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]);
 #pragma unroll
                 for (int ri = 0; ri < 8; ++ri) {
                     const int i = L.row(ri);
                     gstore4(D, ld, n, row0 + i, col0 + L.cB0, true, acc[ri][0], acc[ri][1], acc[ri][2], acc[ri][3]);
                     gstore4(D, ld, n, row0 + i, col0 + L.cB1, true, acc[ri][4], acc[ri][5], acc[ri][6], acc[ri][7]);
                 }
-#pragma unroll
-                for (int ci = 0; ci < 8; ++ci) {
-                    const int k = L.col(ci);
-                    vstore4(cp + (long long)k * npad + row0 + L.rA0, acc[0][ci], acc[1][ci], acc[2][ci], acc[3][ci]);
-                    vstore4(cp + (long long)k * npad + row0 + L.rA1, acc[4][ci], acc[5][ci], acc[6][ci], acc[7][ci]);
-                }
+                store_col_panel(static_cast<T*>(nbuf ? ptrs.colpT[1] : ptrs.colpT[0]), acc, L, row0, npad);
                 continue;
             }
         }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 namespace apsp {
 
@@ -74,6 +75,16 @@ struct FusedArgs {
 // SM splits its tiles by 4, so that it fills the GPU and each round's
 // critical tiles (on the path through phase 1 and phase 2) finish sooner.
 inline int fused_split(int nb, int sms) { return (long long)nb * nb < 4LL * sms ? 4 : 1; }
+
+// Panel layout of the round-fused schedule, per element type.  1: k-major
+// (panel row k holds D[k][j], or D[i][k] for the transposed column panel).
+// 2: k-pair interleaved, element (k, x) at row k / 2, column 2x + k % 2 of a
+// panel twice as wide and half as high, so that phase 3 reads both k-steps
+// of a pair in one 64-bit operand.  fp32 uses 2 (a packed add.rn.f32x2 and
+// a three-input minimum per two relaxations); int32 uses 1 (its fused
+// add-min takes one k-step at a time).
+template <typename T>
+constexpr int kPanelPack = std::is_same<T, float>::value ? 2 : 1;
 
 // Opt the kernels into their shared-memory sizes on the current device.
 template <typename T> cudaError_t kernels_init();
