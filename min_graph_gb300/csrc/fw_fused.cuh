@@ -40,6 +40,10 @@
 //                  accumulators start at INF, the consumers stage the result
 //                  in the C buffer, and the producer merges it into D with a
 //                  TMA min-reduction in L2 (D is never loaded into the SM).
+//                  int32 runs the fused add-min on k-major panels; fp32 runs
+//                  the packed core on k-pair interleaved panels (kPanelPack
+//                  in fw_launch.h), one packed add and one three-input
+//                  minimum per two relaxations.
 //   row panel:     C <- D tile (also the B operand, read in shared memory);
 //                  A slabs <- transposed closed primary tile
 //   column panel:  C <- D tile; the consumers write its transpose into the
@@ -541,7 +545,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
                 if (!mbar_wait_bounded(bar_full + 8 * st, use & 1, err, timeout_ns)) return;
                 const T* As = reinterpret_cast<const T*>(ring + st * FZ_STAGE);
                 if constexpr (kPanelPack<T> == 2)
-                    mm_core<T, kCorePacked, KS>(acc, As, As + KS * TB, L);  // k-pair interleaved slabs
+                    mm_core_packed<T, KS, 2>(acc, As, As + KS * TB, L);  // k-pair interleaved slabs
                 else
                     mm_core_fused<T, KS, 8>(acc, As, As + KS * TB, L);
                 __syncwarp();
