@@ -600,29 +600,56 @@ def ours_johnson(args, rank, world, local):
         src = np.array([0, n // 3, (2 * n) // 3, n - 1], dtype=np.int32)
         check = bool(np.array_equal(work[src.tolist(), :].cpu().numpy(), oracle.dijkstra_i32(w, src)))
 
+    # end to end: each step uploads the dense matrix from pinned host memory,
+    # solves it and downloads the result.  The copies run on a copy stream
+    # into and out of two device buffers, so step b + 1's upload and step
+    # b - 1's download overlap the solve of step b (as the batched host
+    # entry point of the dense solver does).
     e2e = None
     if not args.no_e2e:
         host_src = torch.from_numpy(w)
         pinned = torch.empty_like(host_src).pin_memory()
-        out_host = torch.empty_like(host_src).pin_memory()
-        dev_buf = torch.empty_like(pristine)
-        e2e_times = []
-        for it in range(args.steps + 1):  # the first call warms up
-            pinned.copy_(host_src)
-            barrier()
-            t0 = time.perf_counter()
-            dev_buf.copy_(pinned, non_blocking=True)
-            apsp.solve_sparse(dev_buf, delta=args.delta, stream=stream)
-            out_host.copy_(dev_buf, non_blocking=True)
-            torch.cuda.current_stream(dev).synchronize()
-            if it > 0:
-                e2e_times.append(time.perf_counter() - t0)
-        e2e_total = sum(e2e_times)
-        e2e_total = max_over_ranks(dist, e2e_total, dev)
+        pinned.copy_(host_src)
+        outs = [torch.empty_like(host_src).pin_memory() for _ in range(2)]
+        bufs = [torch.empty_like(pristine) for _ in range(2)]
+        cs = torch.cuda.Stream(dev)
+
+        def pipelined(count):
+            up = [torch.cuda.Event() for _ in range(2)]
+            done = [torch.cuda.Event() for _ in range(2)]
+
+            def upload(b):
+                with torch.cuda.stream(cs):
+                    bufs[b % 2].copy_(pinned, non_blocking=True)
+                    up[b % 2].record(cs)
+
+            upload(0)
+            if count > 1:
+                upload(1)
+            for b in range(count):
+                k = b % 2
+                stream.wait_event(up[k])
+                apsp.solve_sparse(bufs[k], delta=args.delta, stream=stream)  # returns when solved
+                done[k].record(stream)
+                cs.wait_event(done[k])
+                with torch.cuda.stream(cs):
+                    outs[k].copy_(bufs[k], non_blocking=True)  # then step b + 2's upload reuses bufs[k]
+                if b + 2 < count:
+                    upload(b + 2)
+            cs.synchronize()
+            stream.synchronize()
+
+        pipelined(2)  # warm-up
+        barrier()
+        t0 = time.perf_counter()
+        pipelined(args.steps)
+        e2e_total = max_over_ranks(dist, time.perf_counter() - t0, dev)
         nbytes = n * n * 4
         e2e = {"value": whole_job_value(world, args.steps, float(n) ** 3, e2e_total), "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
-               "ms_per_step": e2e_total / args.steps * 1e3}
+               "ms_per_step": e2e_total / args.steps * 1e3,
+               "api": "apsp_solve_sparse_i32 on device buffers; copies on a second stream overlap the neighbouring steps' solves",
+               "result_matches_device_solve": bool(torch.equal(outs[(args.steps - 1) % 2][:4], work[:4].cpu()))}
 
     clk = clocks.summary()
     roof = None
