@@ -1197,28 +1197,55 @@ apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int3
 
 // Partition the arcs against delta, then one persistent search CTA per
 // resident slot.  512 threads a CTA while at least two CTAs fit an SM (n up
-// to about 24K), else 1024 threads in one CTA.
-apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, const int32_t* sources,
-                          int nsrc, int32_t delta, const long long* h, int32_t* out, long long ldo, const Work& wk,
-                          cudaStream_t s) {
+// to about 24K), else 1024 threads in one CTA.  Graphs of at most 8192
+// vertices with a mean out-degree of at most 512 take 256-thread CTAs when
+// there are sources enough to fill them: twice as many searches share an
+// SM, and such a search's phases seldom keep 512 threads busy.  Measured
+// (Johnson, all sources): ER n = 2048, degree 100: 1.185 -> 1.064 ms;
+// n = 8192, degree 4096: 393.8 -> 402.1 ms; n = 256 (256 sources, fewer
+// than the slots): 0.150 -> 0.155 ms.
+apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m,
+                          const int32_t* sources, int nsrc, int32_t delta, const long long* h, int32_t* out,
+                          long long ldo, const Work& wk, cudaStream_t s) {
     apsp_status_t prc = partition_arcs(rp, col, w, n, delta, wk.arcs, wk.nlight, wk.biglist, wk.bigcount, s);
     if (prc != APSP_OK) return prc;
     cudaError_t e;
     const size_t smem = sssp_smem_bytes(n);
-    e = cudaFuncSetAttribute(sssp_delta_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(sssp_delta_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return sp_fail(e);
-    int dev = 0, sms = 0, per_sm = 0;
+    // Kernel attributes and occupancies for this shared-memory size, kept
+    // from the last call on this device (the callers hold g_sp_mu).
+    struct LaunchShape {
+        int dev = -1, sms = 0, per_sm[3] = {0, 0, 0};  // 256, 512, 1024 threads
+        size_t smem = 0;
+    };
+    static LaunchShape shape;
+    int dev = 0;
     e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel<512>, 512, smem);
     if (e != cudaSuccess) return sp_fail(e);
-    const bool wide = n > 1024 * (512 / 32) || per_sm < 2;  // the 512-thread CTA covers n <= 16384
-    if (wide) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sssp_delta_kernel<1024>, 1024, smem);
+    if (shape.dev != dev || shape.smem != smem) {
+        LaunchShape x;
+        e = cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sssp_delta_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sssp_delta_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sssp_delta_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[0], sssp_delta_kernel<256>, 256, smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[1], sssp_delta_kernel<512>, 512, smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[2], sssp_delta_kernel<1024>, 1024, smem);
         if (e != cudaSuccess) return sp_fail(e);
+        x.dev = dev;
+        x.smem = smem;
+        shape = x;
     }
+    const int sms = shape.sms;
+    const bool wide = n > 1024 * (512 / 32) || shape.per_sm[1] < 2;  // the 512-thread CTA covers n <= 16384
+    const bool narrow = !wide && n <= 1024 * (256 / 32) && m <= 512LL * n &&
+                        (long long)nsrc >= (long long)sms * shape.per_sm[0];
+    const int per_sm = shape.per_sm[wide ? 2 : narrow ? 0 : 1];
     if (per_sm < 1) return APSP_EUNSUPPORTED;
     long long grid = (long long)sms * per_sm;
     if (grid > nsrc) grid = nsrc;
@@ -1236,8 +1263,10 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
             return sp_fail(e);
         }
     }
-    apsp_status_t rc = wide ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
-                            : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
+    apsp_status_t rc =
+        wide     ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
+        : narrow ? launch_search<256>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
+                 : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
     count_kernel();  // the search
     if (rc == APSP_OK && ev[1]) {
         e = cudaEventRecord(ev[1], s);
@@ -1308,7 +1337,7 @@ apsp_status_t johnson(const int64_t* rp, const int32_t* col, const int32_t* w, i
         if (rc != APSP_OK) return rc;
     }
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(rp, col, wuse, n, nullptr, n, delta, huse, out, ld, wk, s);
+    return launch_sssp(rp, col, wuse, n, m, nullptr, n, delta, huse, out, ld, wk, s);
 }
 
 // CSR of a dense matrix into st.rp / st.body; returns m.
@@ -1647,7 +1676,7 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
     if (rc != APSP_OK) return rc;
     if (bad || (m > 0 && (lo < 0 || hi >= kInf))) return APSP_EINVAL;
     if (delta <= 0) delta = default_delta(n, m, hi);
-    return launch_sssp(row_ptr, col_idx, w, n, sources, nsrc, delta, nullptr, out, ldo, wk, s);
+    return launch_sssp(row_ptr, col_idx, w, n, m, sources, nsrc, delta, nullptr, out, ldo, wk, s);
 }
 
 apsp_status_t apsp_johnson_csr_i32(const int64_t* row_ptr, const int32_t* col_idx, const int32_t* w, int n,

@@ -308,6 +308,30 @@ def test_dense_rows_take_the_cta_partition():
     assert_i32_exact(got.cpu().numpy(), oracle.dijkstra_i32(w, src), "dense rows")
 
 
+@pytest.mark.parametrize("n", [1000, 4000, 8192])
+def test_low_degree_graphs_take_narrow_search_ctas(n):
+    # at most 8192 vertices, mean degree <= 512 and as many sources as search
+    # slots: the 256-thread search kernel (8192 = its largest n); negative
+    # weights go through the reweighting; rows against the oracle's Johnson
+    w = graphgen.er_potential_i32(n, 8.0 / n, 0, 1000, 2000, seed=n)
+    src = np.array([0, 1, n // 2, n - 1], dtype=np.int32)
+    ref = oracle.johnson_rows_i32(w, src)
+    assert ref is not None and (w[w < INF] < 0).any()
+    t = torch.from_numpy(w).cuda()
+    apsp.solve_sparse(t)
+    got = t[torch.from_numpy(src).long().cuda()].cpu().numpy()
+    assert_i32_exact(got, ref, f"n={n} narrow CTAs")
+
+
+def test_narrow_search_ctas_for_many_sources():
+    # 2000 sources of a 3000-vertex graph of mean degree 9, multi-source entry
+    w = graphgen.er_i32(3000, 0.003, 0, 300, seed=41)
+    rp, col, wt = to_dev(*csr_of(w))
+    src = np.random.default_rng(5).integers(0, 3000, 2000).astype(np.int32)
+    got = apsp.sssp_delta(rp, col, wt, torch.from_numpy(src).cuda())
+    assert_i32_exact(got.cpu().numpy(), oracle.dijkstra_i32(w, src), "2000 sources")
+
+
 def test_negative_weights_above_the_512_thread_limit():
     # n = 17000 takes the 1024-thread search kernel; rows against the
     # oracle's Johnson for sampled sources
