@@ -404,6 +404,7 @@ def ours(args, rank, world, local):
     clk = clocks.summary()
     f_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
     f_load = (clk or {}).get("sm_mhz")
+    f_gemm = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
     fused = phase_cnt[0] == 0 and phase_cnt[2] > 0
     p3_launches = phase_cnt[2]
     p3_ms = phase_ms[2] / p3_launches if p3_launches else None
@@ -433,6 +434,12 @@ def ours(args, rank, world, local):
                     f"{sms} SMs x {NOMINAL_INT32_LANES} INT32 lanes x {f_max:.0f} MHz"
                     + (" / 2 ops per fp32 relaxation" if ops_per_relax == 2 else ""),
                 "frac_at_load_clock": (achieved / (peak_tops * f_load / f_max)) if f_load else None,
+                # the peak at the median SM clock that MEASURED_PEAKS.json saw
+                # under a power-capped bf16 GEMM; this kernel's own clock is
+                # sampled above (clocks.sm_mhz), and `frac` uses the maximum
+                "peak_at_gemm_load_clock": (peak_tops * f_gemm / f_max) if f_gemm else None,
+                "frac_at_gemm_load_clock": (achieved / (peak_tops * f_gemm / f_max)) if f_gemm else None,
+                "gemm_load_clock_mhz": f_gemm,
                 "avg_launch_ms": p3_ms, "launches": p3_launches,
                 "phase_share": [m / sum(phase_ms) for m in phase_ms] if sum(phase_ms) > 0 else None}
         if not fused and phase_cnt[0] > 0 and phase_cnt[1] > 0:
