@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import min_graph_gb300 as apsp
@@ -130,6 +131,22 @@ def test_python_binding_rejects_non_cuda():
         apsp.solve(torch.zeros(4, 4, dtype=torch.int32))
     with pytest.raises(ValueError):
         apsp.solve(torch.zeros(4, 5, dtype=torch.int32))
+
+
+def test_host_batch_binding_checks_its_matrices(libs):
+    # shapes, leading dimensions and dtypes are checked before any CUDA call
+    a4 = np.zeros((4, 4), np.int32)
+    with pytest.raises(ValueError):
+        apsp.solve_host_batch([a4, np.zeros((5, 5), np.int32)])      # sizes differ
+    with pytest.raises(ValueError):
+        apsp.solve_host_batch([a4], [np.zeros((4, 4), np.float32)])  # dtypes differ
+    with pytest.raises(ValueError):
+        apsp.solve_host_batch([a4], [])                             # lengths differ
+    with pytest.raises(ValueError):
+        apsp.solve_host_batch([np.zeros((4, 5), np.int32)])          # not square
+    with pytest.raises(TypeError):
+        apsp.solve_host_batch([np.zeros((4, 4), np.int64)])          # unsupported dtype
+    assert apsp.solve_host_batch([]) == []
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
