@@ -41,6 +41,18 @@ apsp_status_t apsp_debug_inject_phase3_timeout(unsigned long long timeout_ns);
  */
 apsp_status_t apsp_debug_inject_grid_timeout(unsigned long long timeout_ns);
 
+/*
+ * apsp_debug_fail_next_allocations -- make the next `count` device buffer
+ * allocations of the dense entry points (workspace and staging buffers) fail
+ * on the host, as cudaMalloc does when the device is full: no memory is
+ * requested, and the call that needed the buffer returns APSP_ENOMEM with
+ * apsp_last_cuda_error() = cudaErrorMemoryAllocation.  Nothing is enqueued
+ * for that call, and the next call allocates normally.
+ *   count  0 .. 1000 (0 disarms the hook).
+ * Returns APSP_EINVAL for an out-of-range count.
+ */
+apsp_status_t apsp_debug_fail_next_allocations(int count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -94,6 +94,8 @@ def load():
         lib.apsp_debug_inject_phase3_timeout.restype = i32
         lib.apsp_debug_inject_grid_timeout.argtypes = [ctypes.c_ulonglong]
         lib.apsp_debug_inject_grid_timeout.restype = i32
+        lib.apsp_debug_fail_next_allocations.argtypes = [i32]
+        lib.apsp_debug_fail_next_allocations.restype = i32
         lib.apsp_solve_sparse_i32.argtypes = [vp, i32, i32, i32, vp]
         lib.apsp_solve_sparse_i32.restype = i32
         lib.apsp_johnson_csr_i32.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]

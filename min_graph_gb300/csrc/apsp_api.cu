@@ -53,6 +53,7 @@ struct DeviceState {
 std::mutex g_mu;
 std::vector<DeviceState> g_dev;
 int g_inject = 0;  // test hook, consumed by the next persistent phase-3 launch
+int g_fail_allocs = 0;  // test hook: the next this many workspace allocations fail
 unsigned long long g_inject_timeout_ns = 0;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
@@ -116,7 +117,13 @@ apsp_status_t ensure_buffer(DeviceState& st, void** buf, size_t* have, size_t ne
         *buf = nullptr;
         *have = 0;
     }
-    cudaError_t e = cudaMalloc(buf, need);
+    cudaError_t e;
+    if (g_fail_allocs > 0) {  // test hook: this allocation fails as if the device were full
+        --g_fail_allocs;
+        e = cudaErrorMemoryAllocation;
+    } else {
+        e = cudaMalloc(buf, need);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();  // clear the sticky-free allocation error
         *buf = nullptr;
@@ -700,6 +707,13 @@ apsp_status_t apsp_release(void) {
     }
     cudaSetDevice(cur);
     return rc;
+}
+
+apsp_status_t apsp_debug_fail_next_allocations(int count) {
+    if (count < 0 || count > 1000) return APSP_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_fail_allocs = count;
+    return APSP_OK;
 }
 
 apsp_status_t apsp_debug_inject_phase3_timeout(unsigned long long timeout_ns) {

@@ -87,6 +87,9 @@ def test_bad_arguments_rejected_without_cuda(libs):
     assert lib.apsp_debug_inject_phase3_timeout(3 * 10**9) == apsp.EINVAL
     assert lib.apsp_debug_inject_grid_timeout(0) == apsp.EINVAL
     assert lib.apsp_debug_inject_grid_timeout(3 * 10**9) == apsp.EINVAL
+    assert lib.apsp_debug_fail_next_allocations(-1) == apsp.EINVAL
+    assert lib.apsp_debug_fail_next_allocations(1001) == apsp.EINVAL
+    assert lib.apsp_debug_fail_next_allocations(0) == apsp.OK
 
 
 def test_sparse_bad_arguments_rejected_without_cuda(libs):

@@ -245,6 +245,41 @@ def test_host_batch_matches_oracle():
     assert apsp.solve_host_batch([]) == []
 
 
+def test_failed_allocation_reports_enomem_and_recovers():
+    # A host-side hook fails the next device allocation as a full device
+    # would: the solve reports APSP_ENOMEM, leaves the matrix alone, and the
+    # next solve allocates and is exact.
+    lib = apsp.load()
+    w = graphgen.er_i32(300, 0.05, 1, 100, seed=3)
+    ref = oracle.fw_i32(w, threads=threads())
+    w2 = graphgen.er_i32(700, 0.02, 1, 100, seed=4)
+    ref2 = oracle.fw_i32(w2, threads=threads())
+    try:
+        apsp.release()  # the next dense solve must allocate its workspace
+        t = torch.from_numpy(w).cuda()
+        assert lib.apsp_debug_fail_next_allocations(1) == apsp.OK
+        with pytest.raises(apsp.ApspError) as ei:
+            apsp.solve(t)
+        assert ei.value.status == apsp.ENOMEM
+        assert lib.apsp_last_cuda_error() == 2  # cudaErrorMemoryAllocation
+        assert np.array_equal(t.cpu().numpy(), w)
+        apsp.solve(t)
+        apsp.stream_check()
+        assert_i32_exact(t.cpu().numpy(), ref, "solve after a failed allocation")
+        # the host entry point: its staging buffer is the first allocation
+        apsp.release()
+        buf = w2.copy()
+        assert lib.apsp_debug_fail_next_allocations(1) == apsp.OK
+        with pytest.raises(apsp.ApspError) as ei:
+            apsp.solve_host(buf)
+        assert ei.value.status == apsp.ENOMEM
+        assert np.array_equal(buf, w2)
+        apsp.solve_host(buf)
+        assert_i32_exact(buf, ref2, "host solve after a failed allocation")
+    finally:
+        lib.apsp_debug_fail_next_allocations(0)
+
+
 def test_validator_flags():
     w = graphgen.er_i32(300, 0.05, 1, 100, seed=1)
     t = torch.from_numpy(w).cuda()
