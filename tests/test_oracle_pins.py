@@ -122,6 +122,17 @@ def test_generator_splitmix64_known_value():
     assert graphgen.splitmix64_at(0, 1) == 0xE220A8397B1DCDAF
 
 
+def test_generator_configs_are_the_five_workloads():
+    # the five workloads: graph family, size, arc probability or attachment
+    # count, weight range and seed, exactly as stated for the benchmark
+    c = graphgen.CONFIGS
+    assert c["er256"] == {"kind": "er", "n": 256, "p": 0.1, "wlo": 1, "whi": 100, "seed": 1, "dtype": "int32"}
+    assert c["er2048"] == {"kind": "er", "n": 2048, "p": 0.05, "wlo": 1, "whi": 1000, "seed": 2, "dtype": "int32"}
+    assert c["er8192"] == {"kind": "er", "n": 8192, "p": 0.5, "wlo": 1, "whi": 10000, "seed": 3, "dtype": "int32"}
+    assert c["ba16384"] == {"kind": "ba", "n": 16384, "beta": 8, "wlo": 1, "whi": 1000, "seed": 4, "dtype": "int32"}
+    assert c["er32768"] == {"kind": "er", "n": 32768, "p": 0.01, "seed": 5, "dtype": "float32"}
+
+
 def test_generator_shapes():
     w = graphgen.make("er256")
     assert w.shape == (256, 256) and np.all(np.diag(w) == 0)
