@@ -136,6 +136,26 @@ def test_python_binding_rejects_non_cuda():
         apsp.solve(torch.zeros(4, 5, dtype=torch.int32))
 
 
+def test_sparse_and_ooc_bindings_check_their_arguments(libs):
+    # argument errors raise before any CUDA call
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        apsp.solve_sparse(torch.zeros(4, 4, dtype=torch.int32))            # not on the device
+    i64, i32 = torch.zeros(5, dtype=torch.int64), torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        apsp.johnson_csr(i32, i32, i32)                                    # row_ptr not int64
+    with pytest.raises(ValueError):
+        apsp.johnson_csr(i64, i32, i32)                                    # host tensors
+    with pytest.raises(ValueError):
+        apsp.sssp(i64, i32, i32, 0)
+    with pytest.raises(ValueError):
+        apsp.solve_ooc(np.zeros((4, 5), np.int32))                         # not square
+    with pytest.raises(ValueError):
+        apsp.solve_ooc(np.zeros((6, 6), np.int32)[:, ::2])                 # not contiguous
+    with pytest.raises(TypeError):
+        apsp.solve_ooc(np.zeros((4, 4), np.int16))                         # unsupported dtype
+
+
 def test_host_batch_binding_checks_its_matrices(libs):
     # shapes, leading dimensions and dtypes are checked before any CUDA call
     a4 = np.zeros((4, 4), np.int32)
