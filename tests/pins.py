@@ -208,6 +208,12 @@ def check_closed_forms(orc) -> list[str]:
             bad.append(f"closed form: unit weights vs BFS seed {seed} (fw)")
         if not np.array_equal(orc.dijkstra_i32(w, np.arange(150), threads=1).astype(np.int64), hops):
             bad.append(f"closed form: unit weights vs BFS seed {seed} (dijkstra)")
+        # The oracle's own BFS (-1 where unreachable) against the one here.
+        for src in (0, 37, 149):
+            got = orc.bfs_hops_i32(w, src).astype(np.int64)
+            got[got < 0] = INF
+            if not np.array_equal(got, hops[src]):
+                bad.append(f"closed form: oracle BFS hops vs BFS seed {seed} source {src}")
     return bad
 
 

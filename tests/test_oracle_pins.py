@@ -196,6 +196,10 @@ MUTANTS = [
      "out[src] = 0;", "out[src] = 1;"),
     ("dijkstra_csr: last arc of every row skipped",
      "for (int64_t e = row_ptr[u]; e < row_ptr[u + 1]; ++e) {", "for (int64_t e = row_ptr[u]; e < row_ptr[u + 1] - 1; ++e) {"),
+    ("bfs: a new vertex gets its parent's hop count (no + 1)",
+     "hops[v] = hops[u] + 1;", "hops[v] = hops[u];"),
+    ("bfs: arcs read transposed",
+     "(int64_t)w[u * ld + v] < O_INF && hops[v] < 0", "(int64_t)w[v * ld + u] < O_INF && hops[v] < 0"),
 ]
 
 
