@@ -60,9 +60,9 @@ import graphgen  # noqa: E402
 
 METRIC = "APSP relaxations/sec (n³/time) and % of GB300 INT32 add-min peak, 1 GPU"
 UNIT = "relaxations/s"
+OOC_METRIC = METRIC.replace(", 1 GPU", ", out-of-core from host memory, 1 GPU")
 TB = 128
 NOMINAL_INT32_LANES = 128  # INT32 lanes per SM per clock (nominal, one add-min per lane)
-MEASURED_ADDMIN_PER_CLK = 64  # fused add-min issue rate per SM per clock (profiles/relaxation_issue_rate.md)
 
 
 def parse():
@@ -176,28 +176,78 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU side
 
-def cpu_oracle_sample(w: np.ndarray, target_s: float = 12.0, chunk: int = 16):
-    """Time the oracle's untiled Floyd-Warshall (all host cores) on the first
-    k-steps of the full matrix, in chunks of `chunk` steps until about
-    target_s seconds have passed.  Returns (relax/s, steps, seconds, threads)."""
+FW_SAMPLE_RELAX = 4e10  # relaxations per CPU sample: the whole solve when n^3 fits, else n^2 per k-step
+
+
+def fw_sample_ksteps(n: int) -> int:
+    """k-steps in one CPU sample of an n-vertex Floyd-Warshall: all n when
+    n^3 <= FW_SAMPLE_RELAX (the whole solve), else the first S = that budget /
+    n^2.  A fixed count, so that every sample of a workload runs the same
+    steps on the same matrix states and two timings of it compare."""
+    if float(n) ** 3 <= FW_SAMPLE_RELAX:
+        return n
+    return max(1, min(n, int(round(FW_SAMPLE_RELAX / (float(n) * n)))))
+
+
+L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
+
+
+def fw_needs_flush(n: int, itemsize: int) -> bool:
+    """Inputs smaller than the flush buffer are timed after an L2 flush."""
+    return n * n * itemsize < L2_FLUSH_BYTES
+
+
+def fw_config(workload: str, n: int, w: np.ndarray, world: int) -> dict:
+    """The `config` of the Floyd-Warshall lines, shared verbatim by both arms."""
+    nbytes = n * n * w.itemsize
+    if fw_needs_flush(n, w.itemsize):
+        l2 = (f"input {nbytes / 2**20:.2f} MiB < L2: restored from a device copy, then L2 flushed by "
+              f"writing a {L2_FLUSH_BYTES >> 20} MiB buffer, before each step, outside the timed events")
+    else:
+        l2 = (f"input {nbytes / 2**30:.2f} GiB > L2; restored from a device copy before each step, "
+              "outside the timed events")
+    return {"workload": workload, "n": n, "graph": graphgen.describe(workload), "l2": l2,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+def time_fw_sample(w: np.ndarray, ksteps: int, threads: int):
+    """One CPU sample: the oracle's untiled Floyd-Warshall (OpenMP over rows)
+    runs k-steps 0 .. ksteps-1 on a fresh copy of the input (int32 clamped to
+    INF; fp32 as fp64).  Returns (seconds, relaxations in the metric's unit,
+    mean fraction of rows the sampled steps process).  The oracle skips row i
+    of step k while D[i][k] is INF, so the fraction says how much of each
+    step's n^2 it ran; it is counted outside the timed calls."""
     import oracle
 
-    thr = oracle.default_threads()
-    d = np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True)
-    n = d.shape[0]
+    is_i32 = w.dtype == np.int32
+    d = (np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True) if is_i32
+         else np.array(w, dtype=np.float64, copy=True))
     orc = oracle.default()
-    k, dt = 0, 0.0
-    while dt < target_s and k < n:
-        kk = min(n, k + chunk)
+    steps = orc.fw_i32_steps if is_i32 else orc.fw_f64_steps
+    n = d.shape[0]
+    dt, rows = 0.0, 0
+    for k in range(ksteps):
+        col = d[:, k]
+        rows += int(np.count_nonzero(col < graphgen.INF_I32) if is_i32 else np.count_nonzero(np.isfinite(col)))
         t0 = time.perf_counter()
-        orc.fw_i32_steps(d, k, kk, threads=thr)
+        steps(d, k, k + 1, threads=threads)
         dt += time.perf_counter() - t0
-        k = kk
-    return k * float(n) * n / dt, k, dt, thr
+    return dt, ksteps * float(n) * n, rows / (ksteps * float(n))
 
 
-def reference_arm(args, rank):
-    """--impl reference: the oracle as it stands, on the host cores."""
+def fw_sample_text(workload: str, n: int, ksteps: int, is_i32: bool, dense: float, threads: int,
+                   seconds: float) -> str:
+    what = "the whole solve" if ksteps == n else f"the first {ksteps} of {n} k-steps"
+    return (f"{what} of the oracle's untiled Floyd-Warshall ({'int32' if is_i32 else 'fp64'}, "
+            f"OpenMP over rows) on the full n={n} {workload} matrix, from the pristine input each "
+            f"sample; the sampled steps process {dense:.1%} of their rows (the oracle skips rows whose "
+            f"D[i][k] is INF); {seconds:.3g} s timed, {threads} threads")
+
+
+def reference_arm(args, rank, ooc: bool = False):
+    """--impl reference: the oracle as it stands, on the host cores.  Each
+    step is one sample (fw_sample_ksteps) from the pristine input, so every
+    step times the same work."""
     if rank != 0:
         return
     import oracle
@@ -205,41 +255,25 @@ def reference_arm(args, rank):
     w = graphgen.make(args.workload)
     n = w.shape[0]
     is_i32 = w.dtype == np.int32
-    d = (np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True) if is_i32
-         else np.array(w, dtype=np.float64, copy=True))
-    orc = oracle.default()
     thr = args.threads or oracle.default_threads()
-    fw_steps = orc.fw_i32_steps if is_i32 else orc.fw_f64_steps
-    # Each step runs chunks of k-steps (continuing, wrapping around n) until
-    # about 2.5 s have passed, so that W + K steps finish in a few minutes.
-    chunk, k = 8, 0
-    relax = []
-    times = []
+    ks = fw_sample_ksteps(n)
+    times, relax, dense = [], [], []
     for step in range(args.warmup + args.steps):
-        dt, done = 0.0, 0
-        while dt < 2.5:
-            kk = min(n, k + chunk)
-            t0 = time.perf_counter()
-            fw_steps(d, k, kk, threads=thr)
-            dt += time.perf_counter() - t0
-            done += kk - k
-            k = kk % n
+        dt, rx, fr = time_fw_sample(w, ks, thr)
         if step >= args.warmup:
             times.append(dt)
-            relax.append(done * float(n) * n)
+            relax.append(rx)
+            dense.append(fr)
     tot = sum(times)
     value = sum(relax) / tot
-    ks = int(round(sum(relax) / len(relax) / (float(n) * n)))
-    sample = (f"about {ks} Floyd-Warshall k-steps of the untiled triple loop "
-              f"({'int32' if is_i32 else 'fp64'}) on the full n={n} {args.workload} matrix per step "
-              f"(~2.5 s, {thr} threads), n^3 rate extrapolated from them")
+    sample = fw_sample_text(args.workload, n, ks, is_i32, float(np.mean(dense)), thr, tot)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32" if is_i32 else "f64",
+        "impl": "reference", "metric": OOC_METRIC if ooc else METRIC, "value": value, "unit": UNIT,
+        "n_gpus": 1 if ooc else args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32" if is_i32 else "f32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload),
-                   "sample": sample},
+        "config": ooc_config(args, n, args.block or None) if ooc else fw_config(args.workload, n, w, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -325,22 +359,46 @@ def ours(args, rank, world, local):
     nb = -(-n // TB)
     fused_schedule = os.environ.get("APSP_FUSED", "1") != "0"
     launches_per_solve = (nb + 1) if fused_schedule else nb + (2 * nb if nb > 1 else 0)
+    # The tile-product core's relaxation rate on this GPU, measured now by
+    # the issue-rate probe (libapsp_peak: the library's own inner loop on a
+    # shared-memory slab, one 256-thread block per SM): the achievable peak
+    # beside the nominal one.
+    import min_graph_gb300.peak as peak
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    probe_variant = 8 if dtype == torch.int32 else 13  # the core phase 3 runs (fused add-min / packed fp32)
+    probe = peak.measure(probe_variant, sms, 256, 8192)
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    apsp.phase_timing_read()
+    flush = (torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+             if fw_needs_flush(n, w.itemsize) else None)
     barrier()
     with ClockSampler(local) as clocks:
-        apsp.phase_timing_enable(True)
         for k in range(args.steps):
             work.copy_(pristine)  # restore the input (outside the events)
+            if flush is not None:
+                flush.fill_(k)  # evict the input and the workspace from L2
             starts[k].record(stream)
             step_solve()
             ends[k].record(stream)
         barrier()
-        apsp.phase_timing_enable(False)
+    apsp.stream_check(stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # A separate, instrumented pass (not part of the headline): CUDA events
+    # around every launch, which splits a solve into its phases.  The events
+    # between launches hold back the overlap of consecutive launches, so
+    # these launch times are slightly longer than the headline's.
+    apsp.phase_timing_read()
+    apsp.phase_timing_enable(True)
+    for _ in range(min(2, args.steps)):
+        work.copy_(pristine)
+        step_solve()
+    torch.cuda.synchronize()
+    apsp.phase_timing_enable(False)
     apsp.stream_check(stream)
     phase_ms, phase_cnt = apsp.phase_timing_read()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(dist, total_ms, dev)
     relax_per_step = float(n) ** 3
@@ -398,23 +456,30 @@ def ours(args, rank, world, local):
 
     # roofline of the dominant kernel (phase 3): algorithmic relaxations per
     # launch / average launch time, against SMs x 128 lanes x clock
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
     pk = peaks()
     clk = clocks.summary()
     f_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
     f_load = (clk or {}).get("sm_mhz")
     f_gemm = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
     fused = phase_cnt[0] == 0 and phase_cnt[2] > 0
-    p3_launches = phase_cnt[2]
-    p3_ms = phase_ms[2] / p3_launches if p3_launches else None
+    inst_launches = phase_cnt[2]
+    inst_ms = phase_ms[2] / inst_launches if inst_launches else None
     npad = nb * TB
     if fused:
         # round-fused schedule: all of a solve's npad^3 relaxations (phases 1-3)
-        # run in its nb + 1 launches of fw_round_fused
+        # run in its nb + 1 launches of fw_round_fused, which take the whole
+        # solve; the average launch is the timed solves' time over their
+        # launches (the short gaps between launches included)
         kernel = "fw_round_fused"
         p3_relax = float(npad) ** 3 / (nb + 1)
+        p3_launches = args.steps * (nb + 1)
+        p3_ms = sum(step_ms) / p3_launches
+        launch_basis = "timed solves' CUDA events / launches (gaps between launches included)"
     else:
+        # three-kernel schedule: phase 3's own launches, from the
+        # instrumented pass's per-launch events
+        p3_launches, p3_ms = inst_launches, inst_ms
+        launch_basis = "per-launch CUDA events of the instrumented pass"
         kernel = ("fw_phase3_minplus" if os.environ.get("APSP_PHASE3") == "cpasync"
                   else "fw_phase3_persistent")
         p3_relax = float(nb - 1) ** 2 * TB ** 3 if nb > 1 else 0.0
@@ -424,7 +489,7 @@ def ours(args, rank, world, local):
     if p3_ms:
         achieved = p3_relax / (p3_ms * 1e-3) / 1e12
         traffic = phase3_traffic(n) if not fused else fused_traffic(n)
-        measured_tops = sms * MEASURED_ADDMIN_PER_CLK * f_max * 1e6 / 1e12
+        measured_tops = sms * probe["relax_per_clk_sm"] * f_max * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Trelax/s",
                 "frac": achieved / peak_tops, "traffic": traffic,
                 "traffic_unit": "GB per launch (DRAM read + write, scaled from the committed ncu capture)",
@@ -440,7 +505,12 @@ def ours(args, rank, world, local):
                 "peak_at_gemm_load_clock": (peak_tops * f_gemm / f_max) if f_gemm else None,
                 "frac_at_gemm_load_clock": (achieved / (peak_tops * f_gemm / f_max)) if f_gemm else None,
                 "gemm_load_clock_mhz": f_gemm,
-                "avg_launch_ms": p3_ms, "launches": p3_launches,
+                "peak_measured_basis": f"{sms} SMs x {probe['relax_per_clk_sm']:.2f} relaxations/clk/SM "
+                                       f"(issue-rate probe in this run: {probe['what']}) x {f_max:.0f} MHz",
+                "probe": probe,
+                "avg_launch_ms": p3_ms, "launches": p3_launches, "avg_launch_basis": launch_basis,
+                "instrumented_pass": {"avg_launch_ms": inst_ms, "launches": inst_launches,
+                                      "phase_ms": phase_ms, "phase_launches": phase_cnt},
                 "phase_share": [m / sum(phase_ms) for m in phase_ms] if sum(phase_ms) > 0 else None}
         if not fused and phase_cnt[0] > 0 and phase_cnt[1] > 0:
             # the three-kernel schedule times phases 1 and 2 apart: their HBM
@@ -460,11 +530,8 @@ def ours(args, rank, world, local):
         roof["solve_hbm_GBps"] = 2.0 * w.itemsize * float(n) * n * nb / (total_ms / args.steps * 1e-3) / 1e9
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and dtype == torch.int32:
-        v, ksteps, secs, thr = cpu_oracle_sample(w)
-        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"first {ksteps} k-steps of the untiled Floyd-Warshall triple loop on the "
-                         f"full n={n} matrix ({secs:.1f} s, {thr} threads)"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_subprocess(args, steps=4, warmup=1)
 
     if rank == 0:
         line = {
@@ -472,10 +539,7 @@ def ours(args, rank, world, local):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32" if dtype == torch.int32 else "f32",
             "data": "synthetic",
-            "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload),
-                       "l2": f"input {n * n * w.itemsize / 2**30:.2f} GiB > L2; restored from a device "
-                             "copy before each step, outside the timed events",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "config": fw_config(args.workload, n, w, world),
             "pct_int32_addmin_peak": (roof["frac"] * 100) if roof else None,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * launches_per_solve,
@@ -517,6 +581,28 @@ def cpu_dijkstra_sample(w: np.ndarray, target_s: float):
         k = min(n, max(k + 1, int(k * target_s / max(dt, 1e-3))))
 
 
+def johnson_config(args, n: int, m: int, world: int) -> dict:
+    """The `config` of the Johnson lines, shared verbatim by both arms."""
+    return {"workload": args.workload, "n": n, "m": m, "graph": graphgen.describe(args.workload),
+            "algo": "johnson", "delta": args.delta or "library default",
+            "l2": f"input {n * n * 4 / 2**30:.2f} GiB; restored from a device copy before each "
+                  "step, outside the timed events; the output rows go to HBM",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+def cpu_baseline_subprocess(args, steps: int, warmup: int):
+    """A cpu_baseline from the reference arm of the same --algo and workload,
+    run as a fresh process (no CUDA context or torch thread pools in it)."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--algo", args.algo,
+           "--workload", args.workload, "--scale", str(args.scale), "--block", str(args.block),
+           "--steps", str(steps), "--warmup", str(warmup), "--threads", str(args.threads)]
+    p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env)
+    if p.returncode != 0:
+        raise RuntimeError("CPU baseline run failed:\n" + p.stderr[-2000:])
+    return json.loads(p.stdout.strip().splitlines()[-1])["cpu_baseline"]
+
+
 def reference_johnson(args, rank):
     if rank != 0:
         return
@@ -533,14 +619,14 @@ def reference_johnson(args, rank):
             ks.append(k)
     value = sum(float(n) ** 2 * k for k in ks) / sum(secs)
     sample = (f"binary-heap Dijkstra (the oracle's per-source search) from about {int(np.mean(ks))} "
-              f"seeded sources of the n={n} {args.workload} graph per step (~2.5 s, {thr} threads)")
+              f"seeded sources of the n={n} {args.workload} graph per step (~2.5 s, {thr} threads), "
+              f"scaled to n sources; {sum(secs):.1f} s timed")
     line = {
         "impl": "reference", "metric": JOHNSON_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(secs) / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "n": n, "m": arc_count(w), "graph": graphgen.describe(args.workload),
-                   "algo": "johnson", "sample": sample},
+        "config": johnson_config(args, n, arc_count(w), args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -675,21 +761,14 @@ def ours_johnson(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, k, secs, thr = cpu_dijkstra_sample(w, 12.0)
-        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"binary-heap Dijkstra (the oracle's per-source search) from {k} seeded sources "
-                         f"of the n={n} graph ({secs:.1f} s, {thr} threads), scaled to n sources"}
+        cpu = cpu_baseline_subprocess(args, steps=4, warmup=1)
 
     if rank == 0:
         line = {
             "metric": JOHNSON_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-            "config": {"workload": args.workload, "n": n, "m": m, "graph": graphgen.describe(args.workload),
-                       "algo": "johnson", "delta": args.delta or "library default",
-                       "l2": f"input {n * n * 4 / 2**30:.2f} GiB; restored from a device copy before each "
-                             "step, outside the timed events; the output rows go to HBM",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "config": johnson_config(args, n, m, world),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels, "clocks": clk, "check_rows_vs_oracle": check, "step_ms": step_ms,
         }
@@ -716,6 +795,14 @@ def sssp_sources(n: int, count: int, row_ptr: np.ndarray) -> np.ndarray:
     return np.array(out, dtype=np.int32)
 
 
+def sssp_config(args, n: int, m: int, graph_bytes: int, world: int) -> dict:
+    """The `config` of the single-source lines, shared verbatim by both arms."""
+    return {"workload": f"rmat{args.scale}", "n": n, "m": m, "graph": graphgen.describe_rmat(args.scale),
+            "algo": "sssp", "delta": args.delta or "library default",
+            "l2": f"graph {graph_bytes / 2**30:.2f} GiB resident; one seeded random source per step",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
 def reference_sssp(args, rank):
     if rank != 0:
         return
@@ -736,8 +823,7 @@ def reference_sssp(args, rank):
         "impl": "reference", "metric": SSSP_METRIC, "value": value, "unit": "TEPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(secs) / len(secs) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": {"workload": f"rmat{args.scale}", "n": n, "m": m, "graph": graphgen.describe_rmat(args.scale),
-                   "algo": "sssp", "sample": sample},
+        "config": sssp_config(args, n, m, int(row_ptr.nbytes + col.nbytes + w.nbytes), args.gpus),
         "cpu_baseline": {"value": value, "unit": "TEPS", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TEPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -848,11 +934,8 @@ def ours_sssp(args, rank, world, local):
             "metric": SSSP_METRIC, "value": value, "unit": "TEPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-            "config": {"workload": f"rmat{args.scale}", "n": n, "m": m, "graph": graphgen.describe_rmat(args.scale),
-                       "algo": "sssp", "delta": delta_used,
-                       "l2": f"graph {(row_ptr.nbytes + col.nbytes + w.nbytes) / 2**30:.2f} GiB resident; "
-                             "one seeded random source per step",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "config": sssp_config(args, n, m, int(row_ptr.nbytes + col.nbytes + w.nbytes), world),
+            "delta_used": delta_used,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels, "clocks": clk, "check_vs_oracle": check, "step_ms": step_ms,
         }
@@ -863,6 +946,13 @@ def ours_sssp(args, rank, world, local):
 
 
 # ------------------------------------------------------------------ out-of-core arm
+
+def ooc_config(args, n: int, K) -> dict:
+    """The `config` of the out-of-core lines, shared verbatim by both arms."""
+    return {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload), "algo": "ooc",
+            "block": K, "super_rounds": (-(-n // K) if K else None),
+            "host": "pinned; restored before each step, outside the timing", "parallelism": "1 GPU"}
+
 
 def ours_ooc(args, rank, world, local):
     """One host matrix streamed through one GPU: under torchrun only rank 0
@@ -917,19 +1007,14 @@ def ours_ooc(args, rank, world, local):
     nR = -(-n // K) if K else None
     nbytes = n * n * w.itemsize
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and w.dtype == np.int32:
-        v, ksteps, secs, thr = cpu_oracle_sample(w)
-        cpu = {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-               "sample": f"first {ksteps} k-steps of the untiled Floyd-Warshall triple loop on the "
-                         f"full n={n} matrix ({secs:.1f} s, {thr} threads)"}
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_subprocess(args, steps=4, warmup=1)
     line = {
-        "metric": METRIC.replace(", 1 GPU", ", out-of-core from host memory, 1 GPU"), "value": value, "unit": UNIT,
+        "metric": OOC_METRIC, "value": value, "unit": UNIT,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int32" if w.dtype == np.int32 else "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "n": n, "graph": graphgen.describe(args.workload), "algo": "ooc",
-                   "block": K, "super_rounds": nR, "host": "pinned; restored before each step, outside the timing",
-                   "parallelism": "1 GPU"},
+        "config": ooc_config(args, n, K),
         "roofline": {"bound": "alu", "achieved": value / 1e12, "peak": peak_tops, "unit": "Trelax/s",
                      "frac": value / 1e12 / peak_tops, "traffic": None, "kernel": "whole call (minplus_accum_kernel "
                      "and the in-core solver, copies overlapped)"},
@@ -948,7 +1033,7 @@ def main():
     rank, world, local = dist_env()
     if args.algo == "ooc":
         if args.impl == "reference":
-            reference_arm(args, rank)
+            reference_arm(args, rank, ooc=True)
         else:
             ours_ooc(args, rank, world, local)
         return

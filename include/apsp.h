@@ -181,11 +181,18 @@ apsp_status_t apsp_release(void);
  *                        (in stream order) it receives the device error
  *                        word: 0, or APSP's timeout flag if a bounded
  *                        device-side wait ran out (the result is then
- *                        undefined).  NULL skips the copy.
- * Set-up: the first call on each device does a one-time set-up with that
- * device current.  It looks up the scratch array's device address
- * (cudaGetSymbolAddress) and sets the kernels' shared-memory limits.  Make
- * that first call before any stream capture.
+ *                        undefined).  NULL skips the copy.  This is the only
+ *                        way a timeout of this entry point is reported:
+ *                        apsp_stream_check reads the default workspace's
+ *                        error word, not the scratch array's.
+ * Set-up: the first call with n >= 1 on each device does a one-time set-up
+ * with that device current.  It looks up the scratch array's device address
+ * (cudaGetSymbolAddress) and loads every kernel the call launches, setting
+ * their shared-memory limits.  Under lazy module loading this is where the
+ * driver maps the library's device image (the scratch array included), and
+ * that mapping may allocate: make the first call at initialisation time,
+ * with a small n, before memory runs short and before any stream capture.
+ * Later calls allocate nothing.
  * Sharing: all calls share the one array, which keeps the last call's
  * contents; each call clears what must start at zero.  Calls whose work
  * overlaps on the GPU (on different streams, or from different host

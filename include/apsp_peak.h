@@ -1,4 +1,8 @@
 /*
+ * MEASUREMENT TOOLING, not part of libapsp's solving interface: a separate
+ * library (libapsp_peak.so) that the benchmark loads for its roofline
+ * denominators.  No solve entry point depends on it.
+ *
  * libapsp_peak -- microbenchmark of the relaxation step's issue rate on the
  * current GPU, which gives the compute roofline for the min-plus update
  * (phase 3 of blocked Floyd-Warshall).  No page prints this number; the

@@ -10,7 +10,12 @@ namespace apsp {
 
 template <typename T>
 cudaError_t kernels_init_impl() {
-    cudaError_t e = cudaFuncSetAttribute(fw_phase2_panels<T>,
+    // Load phase 1 now too (it needs no attribute): under lazy module loading
+    // a kernel is loaded at its first use, and that load may allocate.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fw_phase1_diag<T>);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fw_phase2_panels<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPhase2Smem);
     if (e != cudaSuccess) return e;
