@@ -33,7 +33,7 @@
 // (r = -1) runs phase 1 and phase 2 of round 0; the last launch runs phase 3
 // only.
 //
-// Each CTA is one producer warp (an elected thread takes items, waits for
+// Each CTA is one producer warpgroup (one thread takes items, waits for
 // their inputs, and issues TMA loads and reductions) and eight consumer
 // warps (the arithmetic, on the tile-product core of mm_core.cuh).
 //   phase-3 tile:  A slabs <- column panel; B slabs <- row panel.  The
@@ -64,7 +64,17 @@ namespace apsp {
 
 constexpr int FZ_STAGES = 4;
 constexpr int FZ_CONSUMERS = 256;
-constexpr int FZ_THREADS = FZ_CONSUMERS + 32;
+// One producer warpgroup, of which one thread works.  Nine warps would put
+// three on one SM sub-partition and cap every thread at 168 registers; with
+// twelve, the producer warpgroup hands registers to the consumers
+// (setmaxnreg) and the consumers' tile product compiles without spills.
+// Measured: ba16384 240.05 -> 237.58 ms, er8192 30.54 -> 30.10 ms.
+constexpr int FZ_THREADS = FZ_CONSUMERS + 128;
+constexpr int FZ_REG_LAUNCH = 168;    // registers per thread at launch (65536 / 384, rounded down to 8)
+constexpr int FZ_REG_CONSUMER = 208;  // per consumer thread after the hand-over
+constexpr int FZ_REG_PRODUCER = 88;   // per producer-warpgroup thread (less spills its item logic)
+static_assert(FZ_CONSUMERS * FZ_REG_CONSUMER + 128 * FZ_REG_PRODUCER <= FZ_THREADS * FZ_REG_LAUNCH,
+              "the register hand-over must fit in what the block is launched with");
 constexpr uint32_t FZ_SLAB = KS * TB * 4;       // 16 KiB
 constexpr uint32_t FZ_STAGE = 2 * FZ_SLAB;      // A half + B half
 constexpr uint32_t FZ_C = TB * TB * 4;          // 64 KiB
@@ -327,6 +337,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
 
     if (tid >= FZ_CONSUMERS) {
         // ================================================== producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(FZ_REG_PRODUCER));
         if (tid != FZ_CONSUMERS) return;
         const uint32_t cdst = smem_u32(cbuf);
         const uint32_t rdst = smem_u32(ring);
@@ -397,7 +408,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             w.crit = kCritNone;
             w.s0 = 0;
             w.s1 = TB / KS;
-            int l = -1;  // the item's index; the slot carries -2 - code for a finisher
+            int l = -1;  // the item's index (-2 - code for a finisher)
             bool stop = false;
             if (nfin == 0) {
                 l = atomicAdd(ptrs.counters + rn, 1);
@@ -436,11 +447,14 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
             }
             if (it > 0 && !mbar_wait_bounded(bar_cempty, (it - 1) & 1, err, timeout_ns)) ok = false;
             if (stop || !ok) {
-                slots[it & 1] = -1;
+                slots[2 * (it & 1)] = -1;
                 mbar_arrive(bar_cfull);  // no bytes expected: releases the consumers
                 break;
             }
-            slots[it & 1] = l;
+            // the consumers get the item decoded: kind, critical class and
+            // slab range in one word, the tile in the other
+            slots[2 * (it & 1)] = w.kind | (w.crit << 4) | (w.s0 << 8) | (w.s1 << 16);
+            slots[2 * (it & 1) + 1] = (w.I << 16) | w.J;
             if (w.kind == kItemP3) {
                 mbar_arrive(bar_cfull);  // no C tile: the consumers start from INF
             } else {
@@ -504,6 +518,7 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     }
 
     // ====================================================== consumers
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(FZ_REG_CONSUMER));
     const MMLayout L(tid);
     const int lane = tid & 31;
     const int pb = r & 1, nbuf = rn & 1;
@@ -511,20 +526,16 @@ fw_round_fused(T* __restrict__ D, long long ld, int n, int r, int nb, int npad, 
     uint32_t staged = 0;  // merge epilogue: tiles staged so far
     for (int it = 0;; ++it) {
         if (!mbar_wait_bounded(bar_cfull, it & 1, err, timeout_ns)) return;
-        const int l = slots[it & 1];
-        if (l == -1) return;
+        const int p0 = slots[2 * (it & 1)];
+        if (p0 == -1) return;
+        const int p1 = slots[2 * (it & 1) + 1];
         FusedItem w;
-        if (l <= -2) {  // finisher of split phase-2 tile `code`
-            const int code = -2 - l;
-            w.kind = kItemFin;
-            w.I = code < nb ? rn : code - nb;
-            w.J = code < nb ? code : rn;
-            w.crit = kCritNone;
-            w.s0 = 0;
-            w.s1 = TB / KS;
-        } else {
-            w = fused_item(l, r, nb, x, split);
-        }
+        w.kind = p0 & 15;
+        w.crit = (p0 >> 4) & 15;
+        w.s0 = (p0 >> 8) & 255;
+        w.s1 = (p0 >> 16) & 255;
+        w.I = (int)((unsigned)p1 >> 16);
+        w.J = p1 & 0xFFFF;
         const int row0 = w.I * TB, col0 = w.J * TB;
 
         if (w.kind == kItemP3) {
