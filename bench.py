@@ -63,6 +63,8 @@ UNIT = "relaxations/s"
 OOC_METRIC = METRIC.replace(", 1 GPU", ", out-of-core from host memory, 1 GPU")
 TB = 128
 NOMINAL_INT32_LANES = 128  # INT32 lanes per SM per clock (nominal, one add-min per lane)
+SMALL_MAX_N = 512  # n at or below which the library solves in one launch of a thread-block cluster
+SMALL_BLOCK = 32   # that kernel's block edge
 
 
 def parse():
@@ -284,7 +286,7 @@ def reference_arm(args, rank, ooc: bool = False):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("fw_kernels.cuh", "fw_fused.cuh", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"):
+    for f in ("fw_kernels.cuh", "fw_fused.cuh", "fw_cluster.cuh", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"):
         with open(os.path.join(ROOT, "min_graph_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -357,8 +359,10 @@ def ours(args, rank, world, local):
     apsp.stream_check(stream)
 
     nb = -(-n // TB)
+    small_path = n <= SMALL_MAX_N and os.environ.get("APSP_SMALL", "1") != "0"
     fused_schedule = os.environ.get("APSP_FUSED", "1") != "0"
-    launches_per_solve = (nb + 1) if fused_schedule else nb + (2 * nb if nb > 1 else 0)
+    launches_per_solve = (1 if small_path else (nb + 1) if fused_schedule
+                          else nb + (2 * nb if nb > 1 else 0))
     # The tile-product core's relaxation rate on this GPU, measured now by
     # the issue-rate probe (libapsp_peak: the library's own inner loop on a
     # shared-memory slab, one 256-thread block per SM): the achievable peak
@@ -465,7 +469,15 @@ def ours(args, rank, world, local):
     inst_launches = phase_cnt[2]
     inst_ms = phase_ms[2] / inst_launches if inst_launches else None
     npad = nb * TB
-    if fused:
+    if small_path:
+        # one launch of the one-cluster kernel: all (32 ceil(n/32))^3
+        # relaxations of the 32-wide blocked solve
+        kernel = "fw_cluster_small"
+        p3_relax = float(SMALL_BLOCK * -(-n // SMALL_BLOCK)) ** 3
+        p3_launches = args.steps
+        p3_ms = sum(step_ms) / p3_launches
+        launch_basis = "timed solves' CUDA events (one launch per solve)"
+    elif fused:
         # round-fused schedule: all of a solve's npad^3 relaxations (phases 1-3)
         # run in its nb + 1 launches of fw_round_fused, which take the whole
         # solve; the average launch is the timed solves' time over their

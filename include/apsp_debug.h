@@ -53,6 +53,17 @@ apsp_status_t apsp_debug_inject_grid_timeout(unsigned long long timeout_ns);
  */
 apsp_status_t apsp_debug_fail_next_allocations(int count);
 
+/*
+ * apsp_debug_small_cluster_size -- the number of CTAs in the thread-block
+ * cluster that solves small matrices (n <= 512) on the current device: 16,
+ * or 8 where the device cannot place a 16-CTA cluster, or 0 where it can
+ * place neither (those solves then take the round schedules).  For tests
+ * and benchmarks.
+ *   is_float  0: the int32 kernel, 1: the fp32 kernel.
+ * Returns the size, or -1 if the device is unsupported or a CUDA call failed.
+ */
+int apsp_debug_small_cluster_size(int is_float);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,6 +96,8 @@ def load():
         lib.apsp_debug_inject_grid_timeout.restype = i32
         lib.apsp_debug_fail_next_allocations.argtypes = [i32]
         lib.apsp_debug_fail_next_allocations.restype = i32
+        lib.apsp_debug_small_cluster_size.argtypes = [i32]
+        lib.apsp_debug_small_cluster_size.restype = i32
         lib.apsp_solve_sparse_i32.argtypes = [vp, i32, i32, i32, vp]
         lib.apsp_solve_sparse_i32.restype = i32
         lib.apsp_johnson_csr_i32.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
@@ -350,6 +352,12 @@ def phase_timing_read():
     cnt = (ctypes.c_longlong * 3)()
     _check(load().apsp_phase_timing_read(ms, cnt), "apsp_phase_timing_read")
     return list(ms), list(cnt)
+
+
+def debug_small_cluster_size(is_float: bool = False) -> int:
+    """CTAs in the cluster that solves n <= 512 on the current device (16, 8,
+    or 0 when neither fits); -1 on an unsupported device."""
+    return int(load().apsp_debug_small_cluster_size(1 if is_float else 0))
 
 
 def debug_inject_phase3_timeout(timeout_ns: int) -> None:

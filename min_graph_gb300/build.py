@@ -24,7 +24,7 @@ LIBS = {
     "libapsp.so": ["apsp_api.cu", "fw_i32.cu", "fw_f32.cu", "noalloc.cu", "sparse.cu", "ooc.cu"],
     "libapsp_peak.so": ["peak.cu"],
 }
-HEADERS = ["fw_kernels.cuh", "fw_fused.cuh", "fw_launch.h", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"]
+HEADERS = ["fw_kernels.cuh", "fw_fused.cuh", "fw_cluster.cuh", "fw_launch.h", "fw_launch_impl.cuh", "mm_core.cuh", "tma.cuh"]
 
 
 def _newest_input(srcs):

@@ -48,6 +48,7 @@ struct DeviceState {
     cudaStream_t copy = nullptr; // copy stream of the batched host solves
     cudaEvent_t bev[5] = {};     // their events: start, uploaded[2], solved[2]
     cudaEvent_t done = nullptr;  // end of the last solve that used ws
+    int small_i32 = -1, small_f32 = -1;  // cluster size of the small-matrix path (-1: not asked yet, 0: none)
 };
 
 std::mutex g_mu;
@@ -219,6 +220,13 @@ bool fused_allowed() {
     return !(v && std::strcmp(v, "0") == 0);
 }
 
+// APSP_SMALL=0 sends small matrices through the round schedules too (for
+// comparison and testing) instead of the one-cluster kernel.
+bool small_allowed() {
+    const char* v = std::getenv("APSP_SMALL");
+    return !(v && std::strcmp(v, "0") == 0);
+}
+
 bool args_ok(const void* p, int n, int ld) {
     if (n < 0 || n > APSP_MAX_N || ld < n) return false;
     if (n > 0 && p == nullptr) return false;
@@ -251,11 +259,41 @@ cudaError_t launch_phase(int phase, const apsp::RoundArgs& a, int r, cudaStream_
     }
 }
 
+// Small matrices: the whole solve as one launch of a thread-block cluster
+// (fw_cluster.cuh).  It needs no workspace.  Returns false (and enqueues
+// nothing) when the path does not apply.
+template <typename T>
+bool solve_small(T* d, int n, int ld, cudaStream_t s, DeviceState& st, apsp_status_t* rc) {
+    if (n > apsp::kSmallMaxN || !small_allowed()) return false;
+    int& cluster = std::is_same<T, float>::value ? st.small_f32 : st.small_i32;
+    if (cluster < 0) cluster = apsp::small_cluster_size<T>();
+    if (cluster <= 0) return false;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) {
+        *rc = cuda_fail(e);
+        return true;
+    }
+    const bool timed = g_timing.enabled && cap == cudaStreamCaptureStatusNone;
+    cudaEvent_t e0 = timed ? timing_event() : nullptr, e1 = timed ? timing_event() : nullptr;
+    if (e0) cudaEventRecord(e0, s);
+    const int vec = ((reinterpret_cast<uintptr_t>(d) & 15u) == 0 && (ld % 4) == 0) ? 1 : 0;
+    e = apsp::launch_small<T>(d, ld, n, vec, cluster, s);
+    if (e0 && e1) {
+        cudaEventRecord(e1, s);
+        g_timing.pending[2].emplace_back(e0, e1);
+    }
+    *rc = e == cudaSuccess ? APSP_OK : cuda_fail(e);
+    return true;
+}
+
 // Enqueue a full solve.  Caller holds g_mu.
 template <typename T>
 apsp_status_t solve_locked(T* d, int n, int ld, cudaStream_t s, DeviceState& st) {
     cudaError_t e = init_kernels<T>(st);
     if (e != cudaSuccess) return cuda_fail(e);
+    apsp_status_t small_rc = APSP_OK;
+    if (solve_small<T>(d, n, ld, s, st, &small_rc)) return small_rc;
     const int nb = (n + kTB - 1) / kTB;
     const int npad = nb * kTB;
     bool fresh = false;
@@ -707,6 +745,15 @@ apsp_status_t apsp_release(void) {
     }
     cudaSetDevice(cur);
     return rc;
+}
+
+int apsp_debug_small_cluster_size(int is_float) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* st = nullptr;
+    if (device_state(&st) != APSP_OK) return -1;
+    int& c = is_float ? st->small_f32 : st->small_i32;
+    if (c < 0) c = is_float ? apsp::small_cluster_size<float>() : apsp::small_cluster_size<int32_t>();
+    return c;
 }
 
 apsp_status_t apsp_debug_fail_next_allocations(int count) {

@@ -96,6 +96,13 @@ template <typename T> cudaError_t launch_phase3(const RoundArgs& a, int r, cudaS
 // cudaSuccess without launching when the launch has no work items.
 template <typename T> cudaError_t launch_fused(const FusedArgs& a, int r, cudaStream_t s);
 
+// Small matrices (n <= kSmallMaxN) run in one launch of a thread-block
+// cluster (fw_cluster.cuh).  small_cluster_size<T>() is the cluster size the
+// current device can place (16, else 8), or 0 if neither.
+constexpr int kSmallMaxN = 512;
+template <typename T> int small_cluster_size();
+template <typename T> cudaError_t launch_small(T* d, long long ld, int n, int vec, int cluster, cudaStream_t s);
+
 // Bytes of workspace the round driver needs for n vertices: the device
 // error word, the panels and primary tiles of the three-kernel schedule,
 // then the second panel buffers, flags and counters of the fused schedule.

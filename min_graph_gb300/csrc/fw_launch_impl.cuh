@@ -2,11 +2,63 @@
 // fw_i32.cu and fw_f32.cu so that the two instantiations compile in parallel.
 #pragma once
 
+#include "fw_cluster.cuh"
 #include "fw_fused.cuh"
 #include "fw_kernels.cuh"
 #include "fw_launch.h"
 
 namespace apsp {
+
+static_assert(kSmallMaxN == SC_MAX_N, "small-matrix limit out of date");
+
+template <typename T>
+cudaError_t small_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int cluster, cudaStream_t s) {
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3((unsigned)cluster);
+    cfg->blockDim = dim3(SC_THREADS);
+    cfg->dynamicSmemBytes = sc_smem_bytes<T>();
+    cfg->stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+    return cudaSuccess;
+}
+
+template <typename T>
+int small_cluster_size_impl() {
+    // 16 CTAs is beyond the portable cluster size: opt in, then ask the
+    // device whether it can place one such cluster at all.
+    if (cudaFuncSetAttribute(fw_cluster_small<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sc_smem_bytes<T>()) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cudaFuncSetAttribute(fw_cluster_small<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+        cudaGetLastError();
+    const int sizes[2] = {16, 8};
+    for (int c : sizes) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        small_config<T>(&cfg, attr, c, nullptr);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fw_cluster_small<T>, &cfg) == cudaSuccess && clusters > 0)
+            return c;
+        cudaGetLastError();
+    }
+    return 0;
+}
+
+template <typename T>
+cudaError_t launch_small_impl(T* d, long long ld, int n, int vec, int cluster, cudaStream_t s) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    small_config<T>(&cfg, attr, cluster, s);
+    return cudaLaunchKernelEx(&cfg, fw_cluster_small<T>, d, ld, n, vec);
+}
 
 template <typename T>
 cudaError_t kernels_init_impl() {
@@ -116,5 +168,10 @@ cudaError_t launch_phase3_impl(const RoundArgs& a, int r, cudaStream_t s) {
     }                                                                                            \
     template <> cudaError_t launch_fused<T>(const FusedArgs& a, int r, cudaStream_t s) {         \
         return launch_fused_impl<T>(a, r, s);                                                    \
+    }                                                                                            \
+    template <> int small_cluster_size<T>() { return small_cluster_size_impl<T>(); }            \
+    template <> cudaError_t launch_small<T>(T* d, long long ld, int n, int vec, int cluster,     \
+                                            cudaStream_t s) {                                    \
+        return launch_small_impl<T>(d, ld, n, vec, cluster, s);                                  \
     }                                                                                            \
     }

@@ -248,16 +248,23 @@ def test_host_batch_matches_oracle():
 def test_failed_allocation_reports_enomem_and_recovers():
     # A host-side hook fails the next device allocation as a full device
     # would: the solve reports APSP_ENOMEM, leaves the matrix alone, and the
-    # next solve allocates and is exact.
+    # next solve allocates and is exact.  A small solve (n <= 512, one
+    # cluster) needs no workspace: it succeeds with the hook armed.
     lib = apsp.load()
-    w = graphgen.er_i32(300, 0.05, 1, 100, seed=3)
+    w = graphgen.er_i32(600, 0.05, 1, 100, seed=3)
     ref = oracle.fw_i32(w, threads=threads())
     w2 = graphgen.er_i32(700, 0.02, 1, 100, seed=4)
     ref2 = oracle.fw_i32(w2, threads=threads())
+    ws = graphgen.er_i32(300, 0.05, 1, 100, seed=5)
+    refs = oracle.fw_i32(ws, threads=threads())
     try:
         apsp.release()  # the next dense solve must allocate its workspace
         t = torch.from_numpy(w).cuda()
         assert lib.apsp_debug_fail_next_allocations(1) == apsp.OK
+        small = torch.from_numpy(ws).cuda()
+        apsp.solve(small)
+        apsp.stream_check()
+        assert_i32_exact(small.cpu().numpy(), refs, "small solve with the allocation hook armed")
         with pytest.raises(apsp.ApspError) as ei:
             apsp.solve(t)
         assert ei.value.status == apsp.ENOMEM
@@ -333,25 +340,30 @@ def test_empty_and_single():
     apsp.solve(t)
 
 
-# Environment settings that select each schedule / phase-3 kernel.
+# Environment settings that select each schedule / phase-3 kernel.  The
+# defaults send n <= 512 to the one-cluster small-matrix kernel; every other
+# variant turns that off (APSP_SMALL=0) so that the round schedules are
+# exercised at these sizes too.
 PHASE3_VARIANTS = [
-    {},                                                # round-fused schedule (default)
-    {"APSP_FUSED_SPLIT": "1"},                         # ... each phase-3 tile one item
-    {"APSP_FUSED_SPLIT": "2"},                         # ... split in two along k
-    {"APSP_FUSED_SPLIT": "4"},                         # ... split in four along k
-    {"APSP_FUSED_OVERLAP": "0"},                       # ... each launch after the previous ends
-    {"APSP_FUSED": "0", "APSP_P3_COLS": "8"},          # three kernels, persistent phase 3
-    {"APSP_FUSED": "0", "APSP_P3_COLS": "4"},          # ... with 512 consumer threads
-    {"APSP_FUSED": "0", "APSP_P3_STAGES": "5"},        # ... with a 5-stage slab ring
-    {"APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},     # ... with the cp.async phase 3
+    {},                                                          # default (one cluster when n <= 512)
+    {"APSP_SMALL": "0"},                                         # round-fused schedule
+    {"APSP_SMALL": "0", "APSP_FUSED_SPLIT": "1"},                # ... each phase-3 tile one item
+    {"APSP_SMALL": "0", "APSP_FUSED_SPLIT": "2"},                # ... split in two along k
+    {"APSP_SMALL": "0", "APSP_FUSED_SPLIT": "4"},                # ... split in four along k
+    {"APSP_SMALL": "0", "APSP_FUSED_OVERLAP": "0"},              # ... each launch after the previous ends
+    {"APSP_SMALL": "0", "APSP_FUSED": "0", "APSP_P3_COLS": "8"},   # three kernels, persistent phase 3
+    {"APSP_SMALL": "0", "APSP_FUSED": "0", "APSP_P3_COLS": "4"},   # ... with 512 consumer threads
+    {"APSP_SMALL": "0", "APSP_FUSED": "0", "APSP_P3_STAGES": "5"},  # ... with a 5-stage slab ring
+    {"APSP_SMALL": "0", "APSP_FUSED": "0", "APSP_PHASE3": "cpasync"},  # ... with the cp.async phase 3
 ]
 
 
 @pytest.mark.parametrize("n", [129, 255, 256, 300, 1000, 2100])
 def test_all_schedules_and_phase3_kernels_agree(n, monkeypatch):
     """Every schedule and phase-3 kernel gives the oracle's result: the
-    round-fused schedule with each split of its phase-3 tiles along k, and
-    the three-kernel schedule with each phase-3 kernel."""
+    one-cluster kernel (n <= 512), the round-fused schedule with each split
+    of its phase-3 tiles along k, and the three-kernel schedule with each
+    phase-3 kernel."""
     w = graphgen.er_i32(n, 0.02, 1, 1000, seed=n + 7)
     ref = oracle.fw_i32(w, threads=threads())
     wf = graphgen.er_f32(n, 0.02, seed=n + 8)
@@ -371,7 +383,8 @@ def test_all_schedules_and_phase3_kernels_agree(n, monkeypatch):
         # schedule forms each candidate sum with the same IEEE add, and a
         # minimum is exact in any order: the fused schedule's packed fp32
         # core and the three-kernel schedule's add-then-min core agree bit
-        # for bit.
+        # for bit.  (The one-cluster kernel blocks by 32, not 128, so its
+        # sums may associate differently: it is held to the tolerance only.)
         if env.get("APSP_FUSED_SPLIT") == "1" or env.get("APSP_FUSED") == "0":
             if unsplit_f is None:
                 unsplit_f = gotf
@@ -412,3 +425,48 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     apsp.stream_check()  # the error word was cleared
     got, _ = gpu_solve(w)  # and the next solve is correct
     assert_i32_exact(got, oracle.fw_i32(w, threads=threads()), "after timeout")
+
+
+SMALL_SIZES = [31, 32, 33, 63, 64, 65, 96, 160, 223, 384, 479, 480, 500, 511, 512, 513]
+
+
+@pytest.mark.parametrize("n", SMALL_SIZES)
+def test_small_cluster_path_around_block_edges(n, monkeypatch):
+    """The one-cluster kernel (n <= 512) around its 32-wide block edges, up
+    to its limit and one past it (n = 513 goes to the round schedule), with
+    dense and sparse graphs, int32 bit-exact and fp32 within tolerance.  The
+    round-fused schedule on the same inputs (APSP_SMALL=0) must agree."""
+    for p in (0.02, 0.5):
+        w = graphgen.er_i32(n, p, 1, 1000, seed=3000 + n)
+        ref = oracle.fw_i32(w, threads=threads())
+        got, pad_ok = gpu_solve(w, ld=n + 3)
+        assert pad_ok
+        assert_i32_exact(got, ref, f"small path n={n} p={p}")
+        monkeypatch.setenv("APSP_SMALL", "0")
+        got_rounds, _ = gpu_solve(w)
+        monkeypatch.delenv("APSP_SMALL")
+        assert_i32_exact(got_rounds, ref, f"round schedule n={n} p={p}")
+        wf = graphgen.er_f32(n, p, seed=4000 + n)
+        gotf, pad_ok = gpu_solve(wf, offset=1)
+        assert pad_ok
+        assert_f32_close(gotf, oracle.fw_f64(wf, threads=threads()), f"small path f32 n={n} p={p}")
+
+
+def test_small_cluster_path_in_a_captured_graph():
+    """The one-cluster launch records into a CUDA graph like the other
+    schedules and replays correctly."""
+    w = graphgen.er_i32(300, 0.05, 1, 1000, seed=77)
+    ref = oracle.fw_i32(w, threads=threads())
+    src = torch.from_numpy(w).cuda()
+    t = src.clone()
+    s = torch.cuda.Stream()
+    apsp.solve(t, stream=s)  # first solve outside the capture (one-time set-up)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        apsp.solve(t, stream=s)
+    for _ in range(2):
+        t.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_i32_exact(t.cpu().numpy(), ref, "graph replay")
