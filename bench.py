@@ -179,16 +179,19 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU side
 
 FW_SAMPLE_RELAX = 4e10  # relaxations per CPU sample: the whole solve when n^3 fits, else n^2 per k-step
+FW_SAMPLE_K0 = 256       # k-steps a partial sample starts after (computed once, untimed)
 
 
-def fw_sample_ksteps(n: int) -> int:
-    """k-steps in one CPU sample of an n-vertex Floyd-Warshall: all n when
-    n^3 <= FW_SAMPLE_RELAX (the whole solve), else the first S = that budget /
-    n^2.  A fixed count, so that every sample of a workload runs the same
-    steps on the same matrix states and two timings of it compare."""
+def fw_sample_plan(n: int):
+    """(k0, S): a CPU sample of an n-vertex Floyd-Warshall times k-steps
+    k0 .. k0+S-1.  The whole solve (0, n) when n^3 <= FW_SAMPLE_RELAX; else
+    S = that budget / n^2 steps starting after the first FW_SAMPLE_K0, whose
+    state is computed once, untimed.  Fixed counts, so every sample of a
+    workload times the same steps on the same matrix states."""
     if float(n) ** 3 <= FW_SAMPLE_RELAX:
-        return n
-    return max(1, min(n, int(round(FW_SAMPLE_RELAX / (float(n) * n)))))
+        return 0, n
+    S = max(1, min(n, int(round(FW_SAMPLE_RELAX / (float(n) * n)))))
+    return max(0, min(FW_SAMPLE_K0, n - S)), S
 
 
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
@@ -212,55 +215,66 @@ def fw_config(workload: str, n: int, w: np.ndarray, world: int) -> dict:
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
-def time_fw_sample(w: np.ndarray, ksteps: int, threads: int):
-    """One CPU sample: the oracle's untiled Floyd-Warshall (OpenMP over rows)
-    runs k-steps 0 .. ksteps-1 on a fresh copy of the input (int32 clamped to
-    INF; fp32 as fp64).  Returns (seconds, relaxations in the metric's unit,
-    mean fraction of rows the sampled steps process).
-
-    The oracle skips row i of step k while D[i][k] is INF (no path i ~> k
-    through earlier vertices yet), which makes the first k-steps of a sparse
-    graph cheap.  A whole solve (ksteps == n) counts n^3, the metric's
-    definition.  A partial sample counts the relaxations the oracle executed
-    (n per processed row), so that its rate estimates a whole solve's n^3
-    rate: on these connected graphs every row is processed once k is past
-    the first few hundred vertices, and a whole solve executes nearly n^3.
-    Rows are counted outside the timed calls."""
+def fw_sample_state(w: np.ndarray, k0: int, threads: int) -> np.ndarray:
+    """The oracle's matrix after its first k0 k-steps (int32 clamped to INF;
+    fp32 as fp64), untimed: the starting state of every partial sample."""
     import oracle
 
     is_i32 = w.dtype == np.int32
     d = (np.array(np.minimum(w, graphgen.INF_I32), dtype=np.int32, copy=True) if is_i32
          else np.array(w, dtype=np.float64, copy=True))
-    orc = oracle.default()
-    steps = orc.fw_i32_steps if is_i32 else orc.fw_f64_steps
+    if k0 > 0:
+        (oracle.default().fw_i32_steps if is_i32 else oracle.default().fw_f64_steps)(d, 0, k0, threads=threads)
+    return d
+
+
+def time_fw_sample(state: np.ndarray, k0: int, ksteps: int, threads: int):
+    """One CPU sample: the oracle's untiled Floyd-Warshall (OpenMP over rows)
+    runs k-steps k0 .. k0+ksteps-1 on a fresh copy of `state`.  Returns
+    (seconds, relaxations in the metric's unit, mean fraction of rows the
+    sampled steps process).
+
+    The oracle skips row i of step k while D[i][k] is INF (no path i ~> k
+    through earlier vertices yet).  A whole solve counts n^3, the metric's
+    definition.  A partial sample counts the relaxations the oracle executed
+    (n per processed row): past the first few hundred k-steps of these
+    connected graphs nearly every row is processed, so that rate estimates a
+    whole solve's n^3 rate.  Rows are counted outside the timed calls."""
+    import oracle
+
+    d = np.array(state, copy=True)
+    is_i32 = d.dtype == np.int32
+    steps = oracle.default().fw_i32_steps if is_i32 else oracle.default().fw_f64_steps
     n = d.shape[0]
     dt, rows = 0.0, 0
-    for k in range(ksteps):
+    for k in range(k0, k0 + ksteps):
         col = d[:, k]
         rows += int(np.count_nonzero(col < graphgen.INF_I32) if is_i32 else np.count_nonzero(np.isfinite(col)))
         t0 = time.perf_counter()
         steps(d, k, k + 1, threads=threads)
         dt += time.perf_counter() - t0
-    units = float(n) ** 3 if ksteps == n else float(rows) * n
+    units = float(n) ** 3 if (k0 == 0 and ksteps == n) else float(rows) * n
     return dt, units, rows / (ksteps * float(n))
 
 
-def fw_sample_text(workload: str, n: int, ksteps: int, is_i32: bool, dense: float, threads: int,
+def fw_sample_text(workload: str, n: int, k0: int, ksteps: int, is_i32: bool, dense: float, threads: int,
                    seconds: float) -> str:
-    head = (f"{'the whole solve' if ksteps == n else f'the first {ksteps} of {n} k-steps'} of the oracle's "
-            f"untiled Floyd-Warshall ({'int32' if is_i32 else 'fp64'}, OpenMP over rows) on the full n={n} "
-            f"{workload} matrix, from the pristine input each sample; {seconds:.3g} s timed, {threads} threads")
-    if ksteps == n:
+    what = ("the whole solve" if (k0 == 0 and ksteps == n)
+            else f"k-steps {k0}..{k0 + ksteps - 1} of {n} (from the state after the first {k0}, computed once, untimed)")
+    head = (f"{what} of the oracle's untiled Floyd-Warshall ({'int32' if is_i32 else 'fp64'}, OpenMP over rows) "
+            f"on the full n={n} {workload} matrix, each sample from a fresh copy; {seconds:.3g} s timed, "
+            f"{threads} threads")
+    if k0 == 0 and ksteps == n:
         return head + "; value = n^3 / time"
     return (head + f"; the sampled steps processed {dense:.1%} of their rows (the oracle skips row i of "
-            "step k while D[i][k] is INF); value = relaxations executed per second, which estimates a "
-            "whole solve's n^3 rate since past its first few hundred k-steps a whole solve of this "
-            "connected graph processes nearly every row")
+            "step k while D[i][k] is INF); value = relaxations executed per second, which estimates a whole "
+            "solve's n^3 rate since past its first few hundred k-steps a whole solve of this connected graph "
+            "processes nearly every row")
 
 
 def reference_arm(args, rank, ooc: bool = False):
     """--impl reference: the oracle as it stands, on the host cores.  Each
-    step is one sample (fw_sample_ksteps) from the pristine input, so every
+    step is one sample (fw_sample_plan) from the same starting state, so every
     step times the same work."""
     if rank != 0:
         return
@@ -270,17 +284,18 @@ def reference_arm(args, rank, ooc: bool = False):
     n = w.shape[0]
     is_i32 = w.dtype == np.int32
     thr = args.threads or oracle.default_threads()
-    ks = fw_sample_ksteps(n)
+    k0, ks = fw_sample_plan(n)
+    state = fw_sample_state(w, k0, thr)
     times, relax, dense = [], [], []
     for step in range(args.warmup + args.steps):
-        dt, rx, fr = time_fw_sample(w, ks, thr)
+        dt, rx, fr = time_fw_sample(state, k0, ks, thr)
         if step >= args.warmup:
             times.append(dt)
             relax.append(rx)
             dense.append(fr)
     tot = sum(times)
     value = sum(relax) / tot
-    sample = fw_sample_text(args.workload, n, ks, is_i32, float(np.mean(dense)), thr, tot)
+    sample = fw_sample_text(args.workload, n, k0, ks, is_i32, float(np.mean(dense)), thr, tot)
     line = {
         "impl": "reference", "metric": OOC_METRIC if ooc else METRIC, "value": value, "unit": UNIT,
         "n_gpus": 1 if ooc else args.gpus, "steps": args.steps, "warmup": args.warmup,
