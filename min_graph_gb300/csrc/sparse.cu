@@ -557,15 +557,19 @@ sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nl
 // that other SMs write is read through L2 (ld.global.cg), never from a stale
 // L1 line.  Arc data is read-only and goes through the read-only path.  A
 // vertex with more than kGridBig arcs in the phase is not walked by its warp
-// alone: its arcs go, in segments of kGridBig, to a grid-wide list.  The
-// phase's barrier then says (OR) whether the list is empty; if not, every
-// warp of the grid takes segments from it through an atomic cursor, and a
-// second barrier closes the phase.  A hub of an R-MAT graph (up to 10^5 -
-// 10^6 arcs) is so spread over the whole GPU.
+// alone: its arcs go, in segments of kGridBig, to a grid-wide list (a warp
+// claims its lanes' slots with one atomic).  The phase's barrier then says
+// (OR) whether the list is empty; if not, the grid's warps share the
+// segments out round-robin, and a second barrier closes the phase.  A hub
+// of an R-MAT graph (up to 10^5 - 10^6 arcs) is so spread over the whole
+// GPU, and so are the many vertices of a few hundred arcs, which a warp
+// walking 32 of them at a time would otherwise hold the phase back for.
+// Measured on R-MAT scale 22: a threshold of 1024 arcs 3.56 ms per search,
+// 256 2.85 ms, 128 2.67 ms, 64 2.97 ms, 32 3.53 ms.
 
 constexpr int kGridThreads = 512;
 constexpr int kGridWarps = kGridThreads / 32;
-constexpr int kGridBig = 1024;
+constexpr int kGridBig = 128;  // arcs above which a vertex's arcs go to the grid-wide list (see below)
 
 struct GridCtrl {
     int any[3];          // OR slots, by barrier index mod 3
@@ -574,8 +578,7 @@ struct GridCtrl {
     unsigned gen;        // barrier generation
     int err;             // 1: a barrier wait ran out
     int big_count;       // segments on the grid-wide list in this phase
-    int big_cursor;      // segments taken from it
-    int pad[5];
+    int pad[6];
 };
 
 struct GridArgs {
@@ -631,10 +634,7 @@ __device__ bool grid_reduce(const GridArgs& a, int& k, int any_in, int32_t min_i
         const unsigned arrived = atomicAdd(&c->arrive, 1u) + 1u;
         if (arrived == gridDim.x) {
             // every other CTA is waiting here, so shared state may be reset
-            if (reset_list) {
-                c->big_count = 0;
-                c->big_cursor = 0;
-            }
+            if (reset_list) c->big_count = 0;
             atomicExch(&c->arrive, 0u);
             __threadfence();
             atomicAdd(&c->gen, 1u);
@@ -708,8 +708,7 @@ __device__ __forceinline__ int32_t relax_run(const int2* __restrict__ arcs, int 
 // lane j holds in `bits` the members of word wbase + j (zero past the end),
 // and the whole warp takes part.  Batches of 32 vertices as in the CTA
 // search; a vertex with more than kGridBig arcs goes to the grid-wide list
-// in segments of kGridBig (its warp walks it itself if the list is full),
-// and `pushed` says whether this lane put any there.
+// in segments of kGridBig, and `pushed` says whether this lane put any there.
 template <bool kLight>
 __device__ int32_t expand_words(const GridArgs& a, long long wbase, uint32_t bits, int& pushed) {
     const int lane = threadIdx.x & 31;
@@ -742,18 +741,43 @@ __device__ int32_t expand_words(const GridArgs& a, long long wbase, uint32_t bit
                     cnt = (int)__ldg(a.rp + v + 1) - r0 - nl;
                 }
                 dv = (uint32_t)ld_cg_i32(a.dist + v);
-                if (cnt > kGridBig) {
-                    const int nseg = (cnt + kGridBig - 1) / kGridBig;
-                    const int slot = atomicAdd(&a.ctrl->big_count, nseg);
-                    if (slot + nseg <= a.big_cap) {
+            }
+            {
+                // vertices with more than kGridBig arcs go to the grid-wide
+                // list, one segment per kGridBig arcs; the warp claims its
+                // lanes' slots with one atomic
+                const int nseg = cnt > kGridBig ? (cnt + kGridBig - 1) / kGridBig : 0;
+                int sincl = nseg;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, sincl, o);
+                    if (lane >= o) sincl += y;
+                }
+                const int stotal = __shfl_sync(0xffffffffu, sincl, 31);
+                if (stotal > 0) {
+                    int sbase = 0;
+                    if (lane == 31) sbase = atomicAdd(&a.ctrl->big_count, stotal);
+                    sbase = __shfl_sync(0xffffffffu, sbase, 31);
+                    const int first = sbase + sincl - nseg;
+                    if (sbase + stotal <= a.big_cap) {
                         for (int q = 0; q < nseg; ++q)
-                            a.big[slot + q] = make_int4((int)dv, beg + q * kGridBig, min(kGridBig, cnt - q * kGridBig), 0);
-                        cnt = 0;
-                        pushed = 1;
+                            a.big[first + q] = make_int4((int)dv, beg + q * kGridBig, min(kGridBig, cnt - q * kGridBig), 0);
+                        if (nseg > 0) {
+                            cnt = 0;
+                            pushed = 1;
+                        }
+                    } else {
+                        // Cannot happen: a phase pushes at most the sum of
+                        // ceil(arcs / kGridBig) over its vertices, within the
+                        // 2 m / kGridBig + 16 slots.  Were it to, the claimed
+                        // slots below the cap get empty segments and the warp
+                        // walks the arcs itself.
+                        for (int q = 0; q < nseg; ++q)
+                            if (first + q < a.big_cap) a.big[first + q] = make_int4(0, 0, 0, 0);
                     }
                 }
             }
-            const uint32_t heavy = __ballot_sync(0xffffffffu, cnt > kGridBig);  // list full: walk here
+            const uint32_t heavy = __ballot_sync(0xffffffffu, cnt > kGridBig);  // not on the list: walk here
             for (uint32_t hb = heavy; hb; hb &= hb - 1) {
                 const int src = __ffs(hb) - 1;
                 best = min(best, relax_run(a.arcs, __shfl_sync(0xffffffffu, beg, src),
@@ -825,15 +849,14 @@ __device__ int32_t expand_grid(const GridArgs& a, uint32_t* set, int& pushed) {
 // segments from the grid-wide list until it is empty (the count is final by
 // then).
 __device__ int32_t drain_grid_list(const GridArgs& a) {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = blockIdx.x * kGridWarps + warp, G = gridDim.x * kGridWarps;
     const int count = min(*reinterpret_cast<volatile int*>(&a.ctrl->big_count), a.big_cap);
     int32_t best = INT_MAX;
-    for (;;) {
-        int idx = 0;
-        if (lane == 0) idx = atomicAdd(&a.ctrl->big_cursor, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        if (idx >= count) break;
-        const int4 e = a.big[idx];
+    // segments are at most kGridBig arcs each: a static round-robin over the
+    // grid's warps balances them without a shared cursor
+    for (int idx = gw; idx < count; idx += G) {
+        const int4 e = __ldcg(a.big + idx);  // written by other CTAs before the barrier
         best = min(best, relax_run(a.arcs, e.y, e.z, (uint32_t)e.x, a.dist, a.queued, a.fresh, lane));
     }
     return best;
@@ -982,7 +1005,6 @@ __global__ void grid_init_kernel(GridArgs a, int src) {
         c->gen = 0u;
         c->err = 0;
         c->big_count = 0;
-        c->big_cursor = 0;
     }
 }
 
