@@ -343,10 +343,14 @@ __device__ __forceinline__ int last_lane_at_or_below(int key, int t) {
 // A warp scan numbers the members 0 .. T-1 and they are taken 32 at a time,
 // so every batch but the last is full: lane k finds the word and the bit of
 // member b + k, loads that vertex's arc range, a second warp scan lays the
-// 32 ranges end to end, and the lanes walk the concatenation in chunks of 32
-// arcs, up to kUnroll chunks with their loads in flight together.  Returns
-// this lane's least distance among its successful relaxations (INT_MAX if
-// none).
+// ranges of at most 64 arcs end to end, and the lanes walk the concatenation
+// in chunks of 32 arcs, up to kUnroll chunks with their loads in flight
+// together; a longer range is then walked by the whole warp alone, so that
+// no lane binary-searches the scan for its arcs.  Measured (Johnson, all
+// sources) against laying every range end to end: BA n = 16384: 17.30 ->
+// 17.03 ms; ER n = 2048, degree 100: 1.06 -> 0.87 ms; ER n = 8192, degree
+// 4096: 397 -> 222 ms.  Returns this lane's least distance among its
+// successful relaxations (INT_MAX if none).
 template <bool kLight, int kWarps, int kUnroll>
 __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restrict__ rp,
                                           const int32_t* __restrict__ nlight, const int2* __restrict__ arcs,
@@ -380,14 +384,18 @@ __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restri
             }
             dv = (uint32_t)dist[v];
         }
-        int incl = cnt;
+        // Vertices of more than kWarpArcs arcs are walked by the whole warp,
+        // one at a time (below); the others' arc ranges are laid end to end.
+        constexpr int kWarpArcs = 64;
+        const int lcnt = cnt <= kWarpArcs ? cnt : 0;
+        int incl = lcnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
         const int total = __shfl_sync(0xffffffffu, incl, 31);
-        const int excl = incl - cnt;
+        const int excl = incl - lcnt;
         for (int base = 0; base < total; base += 32 * kUnroll) {
             int2 a[kUnroll];
             uint32_t d[kUnroll];
@@ -412,6 +420,32 @@ __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restri
                 }
             }
         }
+        for (uint32_t hm = __ballot_sync(0xffffffffu, cnt > kWarpArcs); hm; hm &= hm - 1) {
+            const int src = __ffs(hm) - 1;
+            const int hb = __shfl_sync(0xffffffffu, beg, src);
+            const int hc = __shfl_sync(0xffffffffu, cnt, src);
+            const uint32_t hd = __shfl_sync(0xffffffffu, dv, src);
+            for (int t0 = 0; t0 < hc; t0 += 32 * kUnroll) {
+                int2 a[kUnroll];
+#pragma unroll
+                for (int q = 0; q < kUnroll; ++q) {
+                    const int t = t0 + q * 32 + lane;
+                    a[q] = t < hc ? arcs[hb + t] : make_int2(0, -1);
+                }
+#pragma unroll
+                for (int q = 0; q < kUnroll; ++q) {
+                    if (a[q].y < 0) continue;
+                    const uint32_t sum = hd + (uint32_t)a[q].y;
+                    const int32_t nd = sum >= (uint32_t)kUnreached ? kUnreached : (int32_t)sum;
+                    const int u = a[q].x;
+                    if (nd < dist[u] && nd < atomicMin(dist + u, nd)) {
+                        atomicOr(queued + (u >> 5), 1u << (u & 31));
+                        atomicMin(wmin + (u >> 5), nd);
+                        best = min(best, nd);
+                    }
+                }
+            }
+        }
     }
     return best;
 }
@@ -432,8 +466,8 @@ __device__ __forceinline__ int32_t expand(uint32_t bits, const int64_t* __restri
 // that last selection also yields the least queued distance at or above hi.
 // Then the heavy arcs of R; their successful relaxations, with that least
 // distance, give the next bucket.
-template <int kThreads>
-__global__ void __launch_bounds__(kThreads, 1536 / kThreads)
+template <int kThreads, int kMinBlocks = 1536 / kThreads>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 sssp_delta_kernel(const int64_t* __restrict__ rp, const int32_t* __restrict__ nlight,
                   const int2* __restrict__ arcs, int n, const int32_t* __restrict__ sources, int nsrc,
                   int32_t delta, const long long* __restrict__ h, int32_t* __restrict__ out, long long ldo,
@@ -1234,11 +1268,11 @@ int32_t default_delta(int n, long long m, int wmax, DeltaRule rule = DeltaRule::
     return (int32_t)d;
 }
 
-template <int kThreads>
+template <int kThreads, int kMinBlocks = 1536 / kThreads>
 apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int32_t* sources, int nsrc,
                             int32_t delta, const long long* h, int32_t* out, long long ldo, size_t smem, int grid,
                             cudaStream_t s) {
-    sssp_delta_kernel<kThreads><<<grid, kThreads, smem, s>>>(rp, wk.nlight, wk.arcs, n, sources, nsrc, delta, h,
+    sssp_delta_kernel<kThreads, kMinBlocks><<<grid, kThreads, smem, s>>>(rp, wk.nlight, wk.arcs, n, sources, nsrc, delta, h,
                                                              out, ldo, wk.counter, wk.err);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? APSP_OK : sp_fail(e);
@@ -1252,7 +1286,13 @@ apsp_status_t launch_search(const int64_t* rp, const Work& wk, int n, const int3
 // SM, and such a search's phases seldom keep 512 threads busy.  Measured
 // (Johnson, all sources): ER n = 2048, degree 100: 1.185 -> 1.064 ms;
 // n = 8192, degree 4096: 393.8 -> 402.1 ms; n = 256 (256 sources, fewer
-// than the slots): 0.150 -> 0.155 ms.
+// than the slots): 0.150 -> 0.155 ms.  Where shared memory leaves room for
+// four 512-thread CTAs on an SM, a copy of the kernel compiled for 32
+// registers a thread (four CTAs) runs instead of the one for 40 (three):
+// ER n = 8192, degree 4096: 222 -> 184 ms (20 bytes of spill; with two
+// chunks in flight instead of four, no better spill and 249 ms).  Forced
+// on BA n = 16384, whose 68 KB of shared memory a CTA hold three an SM
+// anyway, the 32-register copy only costs: 17.05 -> 17.91 ms.
 apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* w, int n, long long m,
                           const int32_t* sources, int nsrc, int32_t delta, const long long* h, int32_t* out,
                           long long ldo, const Work& wk, cudaStream_t s) {
@@ -1263,7 +1303,7 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
     // Kernel attributes and occupancies for this shared-memory size, kept
     // from the last call on this device (the callers hold g_sp_mu).
     struct LaunchShape {
-        int dev = -1, sms = 0, per_sm[3] = {0, 0, 0};  // 256, 512, 1024 threads
+        int dev = -1, sms = 0, per_sm[4] = {0, 0, 0, 0};  // 256, 512, 1024 threads; 512 at 32 registers
         size_t smem = 0;
     };
     static LaunchShape shape;
@@ -1285,6 +1325,11 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[1], sssp_delta_kernel<512>, 512, smem);
         if (e == cudaSuccess)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[2], sssp_delta_kernel<1024>, 1024, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sssp_delta_kernel<512, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.per_sm[3], sssp_delta_kernel<512, 4>, 512, smem);
         if (e != cudaSuccess) return sp_fail(e);
         x.dev = dev;
         x.smem = smem;
@@ -1294,7 +1339,8 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
     const bool wide = n > 1024 * (512 / 32) || shape.per_sm[1] < 2;  // the 512-thread CTA covers n <= 16384
     const bool narrow = !wide && n <= 1024 * (256 / 32) && m <= 512LL * n &&
                         (long long)nsrc >= (long long)sms * shape.per_sm[0];
-    const int per_sm = shape.per_sm[wide ? 2 : narrow ? 0 : 1];
+    const bool four = !wide && !narrow && shape.per_sm[3] >= 4;  // shared memory leaves room for four
+    const int per_sm = shape.per_sm[wide ? 2 : narrow ? 0 : four ? 3 : 1];
     if (per_sm < 1) return APSP_EUNSUPPORTED;
     long long grid = (long long)sms * per_sm;
     if (grid > nsrc) grid = nsrc;
@@ -1315,6 +1361,7 @@ apsp_status_t launch_sssp(const int64_t* rp, const int32_t* col, const int32_t* 
     apsp_status_t rc =
         wide     ? launch_search<1024>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
         : narrow ? launch_search<256>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
+        : four   ? launch_search<512, 4>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s)
                  : launch_search<512>(rp, wk, n, sources, nsrc, delta, h, out, ldo, smem, (int)grid, s);
     count_kernel();  // the search
     if (rc == APSP_OK && ev[1]) {
