@@ -54,11 +54,20 @@ apsp_status_t ooc_fail(cudaError_t e) {
     return APSP_ECUDA;
 }
 
+// One 4-byte asynchronous copy global -> shared (cached in L1 and L2).
+__device__ __forceinline__ void cp_async4(uint32_t smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem), "l"(gmem) : "memory");
+}
+
 // C (M x N, ldc) <- min(C, A (x) B) for A = AT^T (AT: K x M, lda) and B
 // (K x N, ldb).  M and N are multiples of 128 and K of 32; every row starts
 // 16-byte aligned.  One CTA per 128 x 128 C tile, k-slabs of 32 staged by
 // cp.async through a 3-deep ring, the same register-blocked tile-product
-// core as the in-core phase 3.
+// cores as the in-core phase 3.  int32 copies 16-byte row pieces into k-major
+// slabs for the fused add-min.  fp32 runs the packed core, whose slabs hold
+// k-pairs interleaved (element (k, i) at (k / 2 * 128 + i) * 2 + k % 2): each
+// element is copied on its own (4 bytes), a warp's 32 copies reading 128
+// consecutive bytes of one panel row.
 template <typename T>
 __global__ void __launch_bounds__(MM_THREADS, 1)
 minplus_accum_kernel(T* __restrict__ C, long long ldc, int tiles_n, const T* __restrict__ AT, long long lda,
@@ -73,13 +82,26 @@ minplus_accum_kernel(T* __restrict__ C, long long ldc, int tiles_n, const T* __r
     const uint32_t sm_base = apsp::smem_u32(sm);
     const uint32_t my_sm = ((tid >> 5) * TB + (tid & 31) * 4) * 4;
     const int kk0 = tid >> 5, c4 = (tid & 31) * 4;
+    constexpr bool kPacked = std::is_same<T, float>::value;
+    static_assert(MM_THREADS == 2 * TB, "the packed copy gives each thread one k parity");
     auto issue = [&](int s, int st) {
-        const uint32_t sa = sm_base + st * 2 * SLAB * 4 + my_sm;
+        if constexpr (kPacked) {
+            const int par = tid / TB, i = tid % TB;  // rows k = 2m + par of the slab, column i
+            const uint32_t sa = sm_base + st * 2 * SLAB * 4 + (i * 2 + par) * 4;
 #pragma unroll
-        for (int m = 0; m < SLAB / 4 / MM_THREADS; ++m) {
-            const long long k = (long long)s * KS + kk0 + m * (MM_THREADS / 32);
-            apsp::cp_async16(sa + m * (MM_THREADS / 32) * TB * 4, AT + k * lda + row0 + c4);
-            apsp::cp_async16(sa + SLAB * 4 + m * (MM_THREADS / 32) * TB * 4, B + k * ldb + col0 + c4);
+            for (int m = 0; m < KS / 2; ++m) {
+                const long long k = (long long)s * KS + 2 * m + par;
+                cp_async4(sa + m * TB * 2 * 4, AT + k * lda + row0 + i);
+                cp_async4(sa + SLAB * 4 + m * TB * 2 * 4, B + k * ldb + col0 + i);
+            }
+        } else {
+            const uint32_t sa = sm_base + st * 2 * SLAB * 4 + my_sm;
+#pragma unroll
+            for (int m = 0; m < SLAB / 4 / MM_THREADS; ++m) {
+                const long long k = (long long)s * KS + kk0 + m * (MM_THREADS / 32);
+                apsp::cp_async16(sa + m * (MM_THREADS / 32) * TB * 4, AT + k * lda + row0 + c4);
+                apsp::cp_async16(sa + SLAB * 4 + m * (MM_THREADS / 32) * TB * 4, B + k * ldb + col0 + c4);
+            }
         }
         apsp::cp_async_commit();
     };
@@ -101,7 +123,10 @@ minplus_accum_kernel(T* __restrict__ C, long long ldc, int tiles_n, const T* __r
         __syncthreads();
         if (s + 2 < nslab) issue(s + 2, (s + 2) % P3_STAGES);
         const T* As = sm + (s % P3_STAGES) * 2 * SLAB;
-        apsp::mm_core<T, apsp::Core<T>::value, KS>(acc, As, As + SLAB, L);
+        if constexpr (kPacked)
+            apsp::mm_core_packed<T, KS, 2>(acc, As, As + SLAB, L);
+        else
+            apsp::mm_core<T, apsp::Core<T>::value, KS>(acc, As, As + SLAB, L);
     }
 #pragma unroll
     for (int ri = 0; ri < 8; ++ri) {
