@@ -121,8 +121,51 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 
+class _Nvml:
+    """Read-only NVML queries through ctypes: the SM clock, its maximum and
+    the active clock-event reasons of one GPU (no setting is changed)."""
+
+    CLOCK_SM = 1  # NVML_CLOCK_SM
+    # clock-event reason bits (nvml.h) that the timing rules watch
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            self.lib.nvmlShutdown()
+            raise OSError("no NVML handle for this GPU")
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        clk, rs = self.ct.c_uint(0), self.ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(clk)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.ct.byref(rs)) != 0:
+            return None
+        return clk.value, rs.value
+
+    def max_sm(self):
+        mx = self.ct.c_uint(0)
+        return mx.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(mx)) == 0 else None
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs.
+    In-process NVML every 0.2 ms (one sample right before and one right
+    after the region as well), so that timed regions of a few milliseconds
+    are covered; nvidia-smi every 200 ms where NVML cannot be loaded."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -132,19 +175,50 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.out = None
+        self.nvml = None
+        self.thread = None
+        self.samples = []
+        self.stop = False
+
+    def _loop(self):
+        while not self.stop:
+            x = self.nvml.sample()
+            if x is not None:
+                self.samples.append(x)
+            time.sleep(0.0002)
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.gpu)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            x = self.nvml.sample()
+            if x is not None:
+                self.samples.append(x)
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            time.sleep(0.02)  # running steadily before the timed region starts
+            return self
         try:
             self.out = open(f"/tmp/apsp_clocks_{os.getpid()}.csv", "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.02)  # started before the timed region
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop = True
+            self.thread.join(timeout=5)
+            x = self.nvml.sample()
+            if x is not None:
+                self.samples.append(x)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -155,6 +229,15 @@ class ClockSampler:
             self.out.close()
 
     def summary(self):
+        if self.nvml is not None:
+            mx = self.nvml.max_sm()
+            self.nvml.close()
+            if not self.samples:
+                return None
+            reasons = sorted({name for _, r in self.samples for bit, name in _Nvml.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(float(c) for c, _ in self.samples),
+                    "sm_max_mhz": float(mx) if mx is not None else None,
+                    "samples": len(self.samples), "reasons": reasons, "source": "nvml, every 0.2 ms"}
         if self.proc is None or self.out is None:
             return None
         rows = []
@@ -173,7 +256,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "reasons": reasons, "source": "nvidia-smi, every 200 ms"}
 
 
 # ------------------------------------------------------------------ CPU side
@@ -380,11 +463,6 @@ def ours(args, rank, world, local):
     def step_solve():
         apsp.solve(work, stream=stream)
 
-    for _ in range(args.warmup):
-        work.copy_(pristine)
-        step_solve()
-    apsp.stream_check(stream)
-
     nb = -(-n // TB)
     small_path = n <= SMALL_MAX_N and os.environ.get("APSP_SMALL", "1") != "0"
     fused_schedule = os.environ.get("APSP_FUSED", "1") != "0"
@@ -404,15 +482,26 @@ def ours(args, rank, world, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     flush = (torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
              if fw_needs_flush(n, w.itemsize) else None)
+
+    def step(k, timed):
+        work.copy_(pristine)  # restore the input (outside the events)
+        if flush is not None:
+            flush.fill_(k)  # evict the input and the workspace from L2
+        if timed:
+            starts[k].record(stream)
+        step_solve()
+        if timed:
+            ends[k].record(stream)
+
+    # warm-up: the timed loop's own sequence, after the probe, so that the
+    # first timed step finds the GPU in the state the others do
+    for k in range(args.warmup):
+        step(k, False)
+    apsp.stream_check(stream)
     barrier()
     with ClockSampler(local) as clocks:
         for k in range(args.steps):
-            work.copy_(pristine)  # restore the input (outside the events)
-            if flush is not None:
-                flush.fill_(k)  # evict the input and the workspace from L2
-            starts[k].record(stream)
-            step_solve()
-            ends[k].record(stream)
+            step(k, True)
         barrier()
     apsp.stream_check(stream)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
