@@ -116,7 +116,10 @@ apsp_status_t apsp_sssp_delta_i32(const int64_t* row_ptr, const int32_t* col_idx
  * weights >= 0 (a negative weight returns APSP_EINVAL), fewer than 2^31 arcs.
  *   dist   device int32[n], 16-byte aligned: the distances from source, INF
  *          for unreachable.  It also serves as the search's working array.
- *   delta  as for apsp_solve_sparse_i32.
+ *   delta  bucket width; <= 0 picks w_max / (2 * mean out-degree).  Past
+ *          the search's peak (a bucket that selected n / 64 vertices or
+ *          more) each bucket is twice as wide as the one before, up to about
+ *          2 * w_max.  Neither delta nor the widening changes the distances.
  * The search is one cooperative launch whose CTAs meet at grid barriers.
  * Every barrier wait is bounded (2 s); one that runs out returns
  * APSP_ETIMEOUT, and dist is then undefined.  Workspace: about 8 bytes per
