@@ -121,14 +121,16 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 
+# NVML clock-event reason bits (nvml.h) that the timing rules watch
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown"}
+
+
 class _Nvml:
     """Read-only NVML queries through ctypes: the SM clock, its maximum and
     the active clock-event reasons of one GPU (no setting is changed)."""
 
     CLOCK_SM = 1  # NVML_CLOCK_SM
-    # clock-event reason bits (nvml.h) that the timing rules watch
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown"}
 
     def __init__(self, index: int):
         import ctypes
@@ -234,7 +236,7 @@ class ClockSampler:
             self.nvml.close()
             if not self.samples:
                 return None
-            reasons = sorted({name for _, r in self.samples for bit, name in _Nvml.REASONS.items() if r & bit})
+            reasons = sorted({name for _, r in self.samples for bit, name in NVML_REASONS.items() if r & bit})
             return {"sm_mhz": statistics.median(float(c) for c, _ in self.samples),
                     "sm_max_mhz": float(mx) if mx is not None else None,
                     "samples": len(self.samples), "reasons": reasons, "source": "nvml, every 0.2 ms"}
